@@ -1,0 +1,58 @@
+"""Bit-level decoders used by the oracle (test infrastructure only).
+
+bf16: the upper 16 bits of an IEEE-754 binary32.
+e4m3 (OCP FP8 "E4M3FN"): 1 sign bit, 4 exponent bits with bias 7, 3 mantissa
+bits; exponent field 0 encodes subnormals m/8 * 2^-6; the single pattern
+S.1111.111 is NaN; there is no infinity; the largest finite magnitude is 448.
+
+FP8 KV row (656 bytes, data and scale adjacent per token, as asked for by
+"Ascend Sparse Attention Forward 算法与优化技术简析", section
+"Decoding KV Cache Layout 优化"): 512 e4m3 latent codes, 4 float32 scales (one
+per 128 latent channels), 64 bf16 rope values.  Group size and rope dtype are
+this library's reading; the page only fixes that data and scale sit together.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+D_V = 512
+D_ROPE = 64
+FP8_GROUP = 128
+FP8_ROW_BYTES = 656
+
+
+def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
+    """Decode raw bf16 bit patterns (uint16/int16 array) exactly to float64."""
+    u32 = bits.astype(np.uint16).astype(np.uint32) << np.uint32(16)
+    return u32.view(np.float32).astype(np.float64)
+
+
+def e4m3_to_f64(codes: np.ndarray) -> np.ndarray:
+    """Decode e4m3 codes (uint8 array) from the format's definition."""
+    c = codes.astype(np.int64)
+    sign = np.where((c >> 7) & 1, -1.0, 1.0)
+    e = (c >> 3) & 0xF
+    m = (c & 0x7).astype(np.float64)
+    normal = (1.0 + m / 8.0) * np.exp2(e.astype(np.float64) - 7.0)
+    sub = (m / 8.0) * 2.0 ** (1 - 7)
+    val = np.where(e == 0, sub, normal)
+    val = np.where((e == 15) & ((c & 7) == 7), np.nan, val)
+    return sign * val
+
+
+def fp8_rows_to_f64(rows: np.ndarray) -> np.ndarray:
+    """Dequantise 656-byte FP8 KV rows [n, 656] (uint8) to float64 [n, 576].
+
+    latent[c] = e4m3(code[c]) * scale[c // 128] (exact in float64);
+    rope = the bf16 values as stored.
+    """
+    rows = np.ascontiguousarray(rows, dtype=np.uint8)
+    n = rows.shape[0]
+    lat = e4m3_to_f64(rows[:, :D_V])
+    scale = rows[:, D_V:D_V + 16].copy().view(np.float32).astype(np.float64)  # [n, 4]
+    lat = lat * np.repeat(scale, FP8_GROUP, axis=1)
+    rope = bf16_bits_to_f64(rows[:, D_V + 16:].copy().view(np.uint16))
+    out = np.empty((n, D_V + D_ROPE), dtype=np.float64)
+    out[:, :D_V] = lat
+    out[:, D_V:] = rope
+    return out
