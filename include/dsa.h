@@ -1,0 +1,125 @@
+/*
+ * dsa.h -- C ABI of the GB300 (sm_103a) DeepSeek Sparse Attention (MLA) forward.
+ *
+ * What is computed ("Ascend Sparse Attention Forward 算法与优化技术简析",
+ * section "数学建模"): for every query token t, with Q_t[h_q, 576],
+ * KV[s_kv, 576], an index list idx_t[topk] and a scalar sm_scale,
+ *
+ *     gathered = KV.index_select(idx_t)                     [topk, 576]
+ *     S        = softmax(sm_scale * Q_t @ gathered^T, -1)   [h_q, topk]
+ *     out_t    = S @ gathered[:, :512]                       [h_q, 512]
+ *     lse_t    = ln(sum(exp(sm_scale * Q_t @ gathered^T)))   [h_q]
+ *
+ * computed blockwise over index blocks of 64 with the online softmax of section
+ * "计算流程": float32 running max / max-for-softmax / sum-of-exp, a float32
+ * output accumulator, a rescale that fires only when the running max has moved
+ * more than 6 (natural-log units) above the max used for the exponentials
+ * ("skip scale"), and S rounded to bf16 before it multiplies V.
+ *
+ * Index semantics: a slot whose value lies outside [0, s_kv) (the -1 marker
+ * included) is excluded exactly; duplicates count once per occurrence; a token
+ * with no valid slot gets out = 0 and lse = -inf.  Slot order does not change
+ * the result beyond rounding.
+ *
+ * Memory: every pointer is a DEVICE pointer owned by the caller.  The library
+ * allocates nothing and keeps no per-call state outside the caller's
+ * workspace.  All calls are asynchronous on `stream`; their return value
+ * reports host-side validation and launch errors only.  A device-side failure
+ * (a bounded wait inside a kernel that gave up) is written to the workspace
+ * and read back with dsa_read_device_status().  No call aborts or throws.
+ *
+ * Layouts (row-major, dense, no padding):
+ *   q        bf16  [s_q, h_q, 576]
+ *   kv       bf16  [s_kv, 576]                          (dsa_sparse_attn_fwd)
+ *            uint8 [s_kv, 656] FP8 rows                 (dsa_sparse_attn_fwd_fp8kv):
+ *                  bytes   0..511  e4m3 latent channels 0..511
+ *                  bytes 512..527  4 x float32 scale, scale g applies to channels 128g..128g+127
+ *                  bytes 528..655  64 x bf16 rope channels 512..575
+ *   indices  int32 [s_q, topk]   global row ids into kv
+ *   out      bf16  [s_q, h_q, 512]
+ *   lse      fp32  [s_q, h_q]    natural-log log-sum-exp of the scaled logits
+ * All pointers must be 16-byte aligned.  Shapes: 0 <= s_q, 1 <= h_q <= 128,
+ * 0 <= s_kv < 2^31, 1 <= topk.
+ */
+#ifndef DSA_GB300_H
+#define DSA_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define DSA_API __attribute__((visibility("default")))
+#else
+#define DSA_API
+#endif
+
+#define DSA_D_QK 576
+#define DSA_D_V 512
+#define DSA_D_ROPE 64
+#define DSA_FP8_ROW_BYTES 656
+#define DSA_MAX_HEADS 128
+#define DSA_B_TOPK 64
+
+typedef enum {
+  DSA_OK = 0,
+  DSA_ERR_INVALID_ARG = 1,    /* a null pointer where data is needed, or a shape out of range */
+  DSA_ERR_UNSUPPORTED = 2,    /* the current device is not sm_103 / lacks the needed resources */
+  DSA_ERR_MISALIGNED = 3,     /* a pointer is not 16-byte aligned */
+  DSA_ERR_CUDA = 4,           /* a CUDA runtime call or kernel launch failed */
+  DSA_ERR_DEVICE_TIMEOUT = 5, /* a bounded wait inside a kernel gave up (read via dsa_read_device_status) */
+  DSA_ERR_WORKSPACE = 6       /* workspace null or smaller than dsa_sparse_attn_fwd_workspace_size() */
+} dsa_status;
+
+typedef enum { DSA_KV_BF16 = 0, DSA_KV_FP8 = 1 } dsa_kv_format;
+
+/* Bytes of device workspace a forward call with these shapes needs on the
+ * current device (scheduler metadata, per-piece partial outputs for tokens
+ * whose index blocks are split across CTA pairs, a status word).  Returns 0 for
+ * invalid shapes.  The workspace needs no initialisation and may be reused by
+ * consecutive calls on one stream; two calls in flight at once need two
+ * workspaces. */
+DSA_API size_t dsa_sparse_attn_fwd_workspace_size(int s_q, int h_q, int topk, int kv_format);
+
+/* The forward with a bf16 KV cache ("数学建模" / "计算流程" sections cited above).
+ * q, kv, indices: inputs (not modified).  out, lse: outputs (fully written for
+ * every token and head < h_q).  sm_scale: multiplier of the logits.
+ * workspace/workspace_bytes: caller-owned scratch of at least
+ * dsa_sparse_attn_fwd_workspace_size(s_q, h_q, topk, DSA_KV_BF16) bytes.
+ * Launches, in order on `stream`: a memset of the workspace's control block,
+ * a counting/scheduling kernel, the attention kernel, and a kernel that merges
+ * the pieces of split tokens. */
+DSA_API dsa_status dsa_sparse_attn_fwd(const void* q, const void* kv, const int32_t* indices, int s_q, int h_q, int s_kv,
+                               int topk, float sm_scale, void* out, float* lse, void* workspace,
+                               size_t workspace_bytes, cudaStream_t stream);
+
+/* The forward with an FP8-e4m3 KV cache of 656-byte rows (layout above; the
+ * per-token data and scales sit together as the page's "Decoding KV Cache
+ * Layout 优化" section asks).  The latent channels are dequantised as
+ * e4m3 * scale and rounded to bf16 before they enter the tensor cores, as the
+ * page's "能不能用 1C1V" section describes for decoding.  Arguments as for
+ * dsa_sparse_attn_fwd, with kv = uint8 [s_kv, 656]. */
+DSA_API dsa_status dsa_sparse_attn_fwd_fp8kv(const void* q, const void* kv_fp8, const int32_t* indices, int s_q, int h_q,
+                                     int s_kv, int topk, float sm_scale, void* out, float* lse, void* workspace,
+                                     size_t workspace_bytes, cudaStream_t stream);
+
+/* Synchronises `stream` and returns the device-side status a previous forward
+ * call left in `workspace` (DSA_OK or DSA_ERR_DEVICE_TIMEOUT), or DSA_ERR_CUDA
+ * if the synchronisation itself failed. */
+DSA_API dsa_status dsa_read_device_status(const void* workspace, cudaStream_t stream);
+
+/* A static, human-readable name for a status code. */
+DSA_API const char* dsa_status_string(dsa_status status);
+
+/* Number of kernels one forward call launches (the memset excluded). */
+DSA_API int dsa_kernels_per_call(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSA_GB300_H */

@@ -1,0 +1,102 @@
+"""Python binding of the C ABI (include/dsa.h): argument marshalling only.
+
+Each function takes torch CUDA tensors, checks dtypes/shapes/contiguity,
+allocates missing outputs and the workspace with torch, and calls the C entry
+point of the same name on the current (or given) stream.  Every step of the
+computation runs in the library's CUDA kernels; there is no other code path.
+"""
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from . import _lib
+
+D_QK = 576
+D_V = 512
+FP8_ROW_BYTES = 656
+KV_BF16 = 0
+KV_FP8 = 1
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def _stream_handle(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def dsa_sparse_attn_fwd_workspace_size(s_q: int, h_q: int, topk: int, kv_format: int = KV_BF16) -> int:
+    return int(_lib.load().dsa_sparse_attn_fwd_workspace_size(s_q, h_q, topk, kv_format))
+
+
+def _check(q, kv, indices, kv_format):
+    if not (q.is_cuda and kv.is_cuda and indices.is_cuda):
+        raise ValueError("q, kv and indices must be CUDA tensors")
+    if q.dtype != torch.bfloat16 or q.dim() != 3 or q.shape[2] != D_QK or not q.is_contiguous():
+        raise ValueError("q must be a contiguous bf16 tensor [s_q, h_q, 576]")
+    if kv_format == KV_BF16:
+        if kv.dtype != torch.bfloat16 or kv.dim() != 2 or kv.shape[1] != D_QK or not kv.is_contiguous():
+            raise ValueError("kv must be a contiguous bf16 tensor [s_kv, 576]")
+    else:
+        if kv.dtype != torch.uint8 or kv.dim() != 2 or kv.shape[1] != FP8_ROW_BYTES or not kv.is_contiguous():
+            raise ValueError("kv must be a contiguous uint8 tensor [s_kv, 656] of FP8 rows")
+    if indices.dtype != torch.int32 or indices.dim() != 2 or indices.shape[0] != q.shape[0] or not indices.is_contiguous():
+        raise ValueError("indices must be a contiguous int32 tensor [s_q, topk]")
+
+
+def _forward(fn_name, kv_format, q, kv, indices, sm_scale, out=None, lse=None, workspace=None, stream=None,
+             check_status=False):
+    _check(q, kv, indices, kv_format)
+    lib = _lib.load()
+    s_q, h_q, _ = q.shape
+    s_kv = kv.shape[0]
+    topk = indices.shape[1]
+    if out is None:
+        out = torch.empty((s_q, h_q, D_V), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((s_q, h_q), dtype=torch.float32, device=q.device)
+    ws_bytes = int(lib.dsa_sparse_attn_fwd_workspace_size(s_q, h_q, topk, kv_format))
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=q.device)
+    st = getattr(lib, fn_name)(_ptr(q), _ptr(kv), _ptr(indices), s_q, h_q, s_kv, topk, ctypes.c_float(sm_scale),
+                               _ptr(out), _ptr(lse), _ptr(workspace), ctypes.c_size_t(workspace.numel()),
+                               _stream_handle(stream))
+    if st != 0:
+        raise _lib.DsaError(st, fn_name)
+    if check_status:
+        dsa_read_device_status(workspace, stream)
+    return out, lse
+
+
+def dsa_sparse_attn_fwd(q, kv, indices, sm_scale, out=None, lse=None, workspace=None, stream=None,
+                        check_status=False):
+    """Sparse MLA forward with a bf16 KV cache.  Returns (out bf16 [s_q,h_q,512], lse f32 [s_q,h_q])."""
+    return _forward("dsa_sparse_attn_fwd", KV_BF16, q, kv, indices, sm_scale, out, lse, workspace, stream,
+                    check_status)
+
+
+def dsa_sparse_attn_fwd_fp8kv(q, kv_fp8, indices, sm_scale, out=None, lse=None, workspace=None, stream=None,
+                              check_status=False):
+    """Sparse MLA forward with an FP8 KV cache of 656-byte rows."""
+    return _forward("dsa_sparse_attn_fwd_fp8kv", KV_FP8, q, kv_fp8, indices, sm_scale, out, lse, workspace, stream,
+                    check_status)
+
+
+def dsa_read_device_status(workspace, stream=None) -> int:
+    """Synchronise the stream and raise if a kernel reported a device-side timeout."""
+    st = int(_lib.load().dsa_read_device_status(_ptr(workspace), _stream_handle(stream)))
+    if st != 0:
+        raise _lib.DsaError(st, "device status")
+    return st
+
+
+def dsa_status_string(code: int) -> str:
+    return _lib.load().dsa_status_string(code).decode()
+
+
+def dsa_kernels_per_call() -> int:
+    return int(_lib.load().dsa_kernels_per_call())

@@ -1,0 +1,304 @@
+// C ABI of the sparse MLA forward (see include/dsa.h), the scheduling kernel
+// that counts valid index slots and lays out the work sequence, and the kernel
+// that merges the pieces of tokens split across CTA pairs.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+
+#include "../../include/dsa.h"
+#include "dsa_internal.h"
+
+namespace dsa {
+
+int fwd_max_active_pairs();
+cudaError_t launch_fwd_bf16(const CUtensorMap& tmap, const FwdParams& p, cudaStream_t stream);
+int fwd_fp8_max_active_pairs();
+cudaError_t launch_fwd_fp8(const FwdParams& p, cudaStream_t stream);
+
+// ----------------------------------------------------------------------------
+// Scheduling: n_valid per token, then (by the last CTA to finish) the prefix
+// sum of index blocks per token, max(1, ceil(n_valid / 64)).  A token with no
+// valid slot still owns one (fully masked) block, which writes out = 0 and
+// lse = -inf.  Per-CTA load balance follows the weight idea of
+// "Flash Attention Infer算子性能优化", section "优化多核负载均衡": work is
+// weighted by valid blocks, and the pairs take equal contiguous shares.
+// ----------------------------------------------------------------------------
+constexpr int kPrepWarps = 8;
+
+__global__ void __launch_bounds__(kPrepWarps * 32) dsa_prep_kernel(const int32_t* __restrict__ indices, int s_q,
+                                                                   int topk, int s_kv, int* nvalid, int* cum,
+                                                                   int* ctrl) {
+  __shared__ int is_last;
+  __shared__ int part[kPrepWarps * 32];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * kPrepWarps + warp;
+  if (t < s_q) {
+    const int32_t* row = indices + (size_t)t * topk;
+    int c = 0;
+    for (int i = lane; i < topk; i += 32) {
+      const int v = __ldg(row + i);
+      c += (v >= 0 && v < s_kv) ? 1 : 0;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
+    if (lane == 0) nvalid[t] = c;
+  }
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) is_last = (atomicAdd(&ctrl[kCtrlTicket], 1) == (int)gridDim.x - 1);
+  __syncthreads();
+  if (!is_last) return;
+  __threadfence();
+  // exclusive scan of blocks-per-token over all tokens (one CTA)
+  const int nthr = blockDim.x;
+  const int per = (s_q + nthr - 1) / nthr;
+  const int t0 = threadIdx.x * per, t1 = min(s_q, t0 + per);
+  int local = 0;
+  for (int i = t0; i < t1; ++i) {
+    const int nv = __ldcg(nvalid + i);
+    local += max(1, (nv + kBT - 1) / kBT);
+  }
+  part[threadIdx.x] = local;
+  __syncthreads();
+  for (int off = 1; off < nthr; off <<= 1) {
+    const int v = threadIdx.x >= off ? part[threadIdx.x - off] : 0;
+    __syncthreads();
+    part[threadIdx.x] += v;
+    __syncthreads();
+  }
+  int run = part[threadIdx.x] - local;  // exclusive prefix
+  for (int i = t0; i < t1; ++i) {
+    cum[i] = run;
+    const int nv = __ldcg(nvalid + i);
+    run += max(1, (nv + kBT - 1) / kBT);
+  }
+  if (threadIdx.x == nthr - 1) {
+    cum[s_q] = part[nthr - 1];
+    ctrl[kCtrlTotalBlocks] = part[nthr - 1];
+  }
+}
+
+// ----------------------------------------------------------------------------
+// Merge of split tokens.  Each piece j of a token holds out_j = O_j / Z_j
+// (normalised over its own blocks) and lse_j = ln Z_j (plus its max); then
+//   lse = ln sum_j exp(lse_j),   out = sum_j exp(lse_j - lse) * out_j.
+// This step is not on the pages; it makes the blockwise result of several
+// pair ranges equal to the result of one range (same exact value).
+// CTA p handles the token containing boundary b_p = p*T/P when b_p is the first
+// boundary strictly inside it.
+// ----------------------------------------------------------------------------
+__device__ __forceinline__ long long boundary(int p, long long T, int P) { return (long long)p * T / P; }
+
+__global__ void __launch_bounds__(256) dsa_combine_kernel(const int* __restrict__ cum, const int* __restrict__ ctrl,
+                                                          int s_q, int h_q, int npairs,
+                                                          const float* __restrict__ part_lse,
+                                                          const float* __restrict__ part_o, uint16_t* out, float* lse) {
+  const int p = blockIdx.x;
+  if (p == 0) return;
+  const long long T = ctrl[kCtrlTotalBlocks];
+  const long long bp = boundary(p, T, npairs);
+  if (bp >= T) return;
+  int lo = 0, hi = s_q - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (cum[mid] <= bp) lo = mid; else hi = mid - 1;
+  }
+  const int t = lo;
+  const long long c0 = cum[t], c1 = cum[t + 1];
+  if (bp == c0) return;                              // boundary at a token start: nothing split here
+  if (boundary(p - 1, T, npairs) > c0) return;       // an earlier boundary inside t handles it
+  // pairs covering blocks c0 .. c1-1: pair(g) = ((g + 1) * P - 1) / T
+  const int pfirst = (int)(((c0 + 1) * npairs - 1) / T);
+  const int plast = (int)((c1 * npairs - 1) / T);
+  constexpr int kMaxPieces = 64;
+  __shared__ int slots[kMaxPieces];
+  __shared__ int nslots;
+  if (threadIdx.x == 0) {
+    int ns = 0;
+    for (int q = pfirst; q <= plast && ns < kMaxPieces; ++q) {
+      const long long bq = boundary(q, T, npairs), bq1 = boundary(q + 1, T, npairs);
+      if (bq1 <= bq) continue;                       // empty range
+      slots[ns++] = (bq >= c0) ? 2 * q : 2 * q + 1;  // t is q's first token iff q starts inside t
+    }
+    nslots = ns;
+  }
+  __syncthreads();
+  const int ns = nslots;
+  for (int h = 0; h < h_q; ++h) {
+    float m = -INFINITY;
+    for (int j = 0; j < ns; ++j) m = fmaxf(m, part_lse[(size_t)slots[j] * h_q + h]);
+    float wsum = 0.f;
+    float w[kMaxPieces];
+    for (int j = 0; j < ns; ++j) {
+      const float l = part_lse[(size_t)slots[j] * h_q + h];
+      w[j] = (m == -INFINITY) ? 0.f : expf(l - m);
+      wsum += w[j];
+    }
+    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+    for (int d = threadIdx.x; d < kDV; d += blockDim.x) {
+      float acc = 0.f;
+      for (int j = 0; j < ns; ++j) acc += w[j] * part_o[((size_t)slots[j] * h_q + h) * kDV + d];
+      out[((size_t)t * h_q + h) * kDV + d] = __bfloat16_as_ushort(__float2bfloat16_rn(acc * inv));
+    }
+    if (threadIdx.x == 0) lse[(size_t)t * h_q + h] = (wsum > 0.f) ? m + logf(wsum) : -INFINITY;
+  }
+}
+
+// Output for s_kv == 0: no row can be valid.
+__global__ void dsa_fill_empty_kernel(uint16_t* out, float* lse, size_t n_out, size_t n_lse) {
+  const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const size_t stride = (size_t)gridDim.x * blockDim.x;
+  for (size_t k = i; k < n_out; k += stride) out[k] = 0;
+  for (size_t k = i; k < n_lse; k += stride) lse[k] = -INFINITY;
+}
+
+static PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    cudaDriverEntryPointQueryResult q;
+    void* f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = (PFN_cuTensorMapEncodeTiled_v12000)f;
+  }
+  return fn;
+}
+
+static bool device_ok() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  int major = 0, minor = 0;
+  cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+  cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+  return major == 10 && minor == 3;
+}
+
+static int pairs_for(int kv_format) {
+  return kv_format == DSA_KV_FP8 ? fwd_fp8_max_active_pairs() : fwd_max_active_pairs();
+}
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+static dsa_status forward(int kv_format, const void* q, const void* kv, const int32_t* indices, int s_q, int h_q,
+                          int s_kv, int topk, float sm_scale, void* out, float* lse, void* workspace,
+                          size_t workspace_bytes, cudaStream_t stream) {
+  if (s_q < 0 || h_q < 1 || h_q > kMaxHeads || s_kv < 0 || topk < 1 || !std::isfinite(sm_scale))
+    return DSA_ERR_INVALID_ARG;
+  if (s_q == 0) return DSA_OK;
+  if (!q || !indices || !out || !lse || (s_kv > 0 && !kv)) return DSA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(out) || !aligned16(lse) || !aligned16(indices) || (kv && !aligned16(kv)))
+    return DSA_ERR_MISALIGNED;
+  if (!device_ok()) return DSA_ERR_UNSUPPORTED;
+  const int npairs = pairs_for(kv_format);
+  if (npairs <= 0) return DSA_ERR_UNSUPPORTED;
+  const WorkspaceLayout L = workspace_layout(s_q, h_q, npairs);
+  if (!workspace || workspace_bytes < L.total || !aligned16(workspace)) return DSA_ERR_WORKSPACE;
+  if (s_kv == 0) {
+    if (cudaMemsetAsync(workspace, 0, 256, stream) != cudaSuccess) return DSA_ERR_CUDA;
+    const size_t n_out = (size_t)s_q * h_q * kDV, n_lse = (size_t)s_q * h_q;
+    dsa_fill_empty_kernel<<<256, 256, 0, stream>>>((uint16_t*)out, lse, n_out, n_lse);
+    return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+  }
+
+  uint8_t* ws = (uint8_t*)workspace;
+  FwdParams p;
+  p.q = (const uint16_t*)q;
+  p.kv = (const uint8_t*)kv;
+  p.indices = indices;
+  p.out = (uint16_t*)out;
+  p.lse = lse;
+  p.s_q = s_q;
+  p.h_q = h_q;
+  p.s_kv = s_kv;
+  p.topk = topk;
+  p.scale_log2 = sm_scale * 1.4426950408889634f;
+  p.ctrl = (int*)(ws + L.ctrl);
+  p.nvalid = (int*)(ws + L.nvalid);
+  p.cum = (int*)(ws + L.cum);
+  p.part_lse = (float*)(ws + L.part_lse);
+  p.part_o = (float*)(ws + L.part_o);
+  p.npairs = npairs;
+
+  if (cudaMemsetAsync(p.ctrl, 0, 256, stream) != cudaSuccess) return DSA_ERR_CUDA;
+  const int prep_blocks = (s_q + kPrepWarps - 1) / kPrepWarps;
+  dsa_prep_kernel<<<prep_blocks, kPrepWarps * 32, 0, stream>>>(indices, s_q, topk, s_kv, p.nvalid, p.cum, p.ctrl);
+  if (cudaGetLastError() != cudaSuccess) return DSA_ERR_CUDA;
+
+  cudaError_t e;
+  if (kv_format == DSA_KV_BF16) {
+    auto encode = get_encode_fn();
+    if (!encode) return DSA_ERR_UNSUPPORTED;
+    CUtensorMap tmap;
+    cuuint64_t dims[2] = {(cuuint64_t)kDQK, (cuuint64_t)s_kv};
+    cuuint64_t strides[1] = {(cuuint64_t)kDQK * 2};
+    cuuint32_t box[2] = {64, 1};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult cr = encode(&tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(kv), dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (cr != CUDA_SUCCESS) return DSA_ERR_CUDA;
+    e = launch_fwd_bf16(tmap, p, stream);
+  } else {
+    e = launch_fwd_fp8(p, stream);
+  }
+  if (e != cudaSuccess) return DSA_ERR_CUDA;
+  dsa_combine_kernel<<<npairs, 256, 0, stream>>>(p.cum, p.ctrl, s_q, h_q, npairs, p.part_lse, p.part_o,
+                                                 (uint16_t*)out, lse);
+  return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+}
+
+}  // namespace dsa
+
+extern "C" {
+
+size_t dsa_sparse_attn_fwd_workspace_size(int s_q, int h_q, int topk, int kv_format) {
+  if (s_q < 0 || h_q < 1 || h_q > dsa::kMaxHeads || topk < 1) return 0;
+  if (kv_format != DSA_KV_BF16 && kv_format != DSA_KV_FP8) return 0;
+  const int npairs = dsa::pairs_for(kv_format);
+  if (npairs <= 0) return 0;
+  return dsa::workspace_layout(s_q, h_q, npairs).total;
+}
+
+dsa_status dsa_sparse_attn_fwd(const void* q, const void* kv, const int32_t* indices, int s_q, int h_q, int s_kv,
+                               int topk, float sm_scale, void* out, float* lse, void* workspace,
+                               size_t workspace_bytes, cudaStream_t stream) {
+  return dsa::forward(DSA_KV_BF16, q, kv, indices, s_q, h_q, s_kv, topk, sm_scale, out, lse, workspace,
+                      workspace_bytes, stream);
+}
+
+dsa_status dsa_sparse_attn_fwd_fp8kv(const void* q, const void* kv_fp8, const int32_t* indices, int s_q, int h_q,
+                                     int s_kv, int topk, float sm_scale, void* out, float* lse, void* workspace,
+                                     size_t workspace_bytes, cudaStream_t stream) {
+  return dsa::forward(DSA_KV_FP8, q, kv_fp8, indices, s_q, h_q, s_kv, topk, sm_scale, out, lse, workspace,
+                      workspace_bytes, stream);
+}
+
+dsa_status dsa_read_device_status(const void* workspace, cudaStream_t stream) {
+  if (!workspace) return DSA_ERR_WORKSPACE;
+  int st = 0;
+  if (cudaMemcpyAsync(&st, workspace, sizeof(int), cudaMemcpyDeviceToHost, stream) != cudaSuccess) return DSA_ERR_CUDA;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return DSA_ERR_CUDA;
+  return (dsa_status)st;
+}
+
+const char* dsa_status_string(dsa_status s) {
+  switch (s) {
+    case DSA_OK: return "DSA_OK";
+    case DSA_ERR_INVALID_ARG: return "DSA_ERR_INVALID_ARG";
+    case DSA_ERR_UNSUPPORTED: return "DSA_ERR_UNSUPPORTED";
+    case DSA_ERR_MISALIGNED: return "DSA_ERR_MISALIGNED";
+    case DSA_ERR_CUDA: return "DSA_ERR_CUDA";
+    case DSA_ERR_DEVICE_TIMEOUT: return "DSA_ERR_DEVICE_TIMEOUT";
+    case DSA_ERR_WORKSPACE: return "DSA_ERR_WORKSPACE";
+  }
+  return "DSA_ERR_UNKNOWN";
+}
+
+int dsa_kernels_per_call(void) { return 3; }
+
+}  // extern "C"

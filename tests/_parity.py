@@ -1,0 +1,61 @@
+"""Helpers for GPU-vs-oracle parity tests (tolerances written here, used by every test).
+
+Tolerances: lse within 2e-3 absolute; out max-abs error <= 1e-2 * max|out_ref| + 1e-3
+for a bf16 KV cache and <= 3e-2 * max|out_ref| for an FP8 cache (the oracle is fed
+the dequantised rows, so the FP8 bound covers the bf16 rounding of the dequantised
+values before the tensor cores).
+"""
+import numpy as np
+import torch
+
+from oracle import dsa_oracle as O
+
+LSE_ABS = 2e-3
+OUT_REL_BF16, OUT_ABS_BF16 = 1e-2, 1e-3
+OUT_REL_FP8, OUT_ABS_FP8 = 3e-2, 0.0
+
+
+def bits(t: torch.Tensor) -> np.ndarray:
+    return t.contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
+
+
+def kv_raw(wl) -> np.ndarray:
+    return wl.kv.numpy() if wl.kv_format == "fp8" else bits(wl.kv)
+
+
+def oracle(wl, tokens=None):
+    tokens = list(range(wl.s_q)) if tokens is None else list(tokens)
+    return O.sparse_mla_fwd_sampled(bits(wl.q), kv_raw(wl), wl.kv_format, wl.indices.numpy(), wl.sm_scale, tokens)
+
+
+def run_gpu(wl, device="cuda"):
+    from sparse_mla_attention_dsa_gb300 import api
+    q = wl.q.to(device)
+    kv = wl.kv.to(device)
+    idx = wl.indices.to(device)
+    fn = api.dsa_sparse_attn_fwd if wl.kv_format == "bf16" else api.dsa_sparse_attn_fwd_fp8kv
+    out, lse = fn(q, kv, idx, wl.sm_scale, check_status=True)
+    torch.cuda.synchronize()
+    return out, lse
+
+
+def compare(out_gpu, lse_gpu, ref_out, ref_lse, kv_format="bf16"):
+    """Returns (ok, report) for GPU outputs (torch, any device) against float64 references."""
+    o = out_gpu.float().cpu().numpy().astype(np.float64)
+    l = lse_gpu.float().cpu().numpy().astype(np.float64)
+    fin = np.isfinite(ref_lse)
+    rep = {}
+    ok = bool(np.array_equal(np.isfinite(l), fin))
+    rep["lse_inf_match"] = ok
+    if fin.any():
+        rep["lse_err"] = float(np.max(np.abs(l[fin] - ref_lse[fin])))
+        ok &= rep["lse_err"] <= LSE_ABS
+    ok &= bool(np.all(np.isneginf(l[~fin])))
+    ref_max = float(np.max(np.abs(ref_out), initial=0.0))
+    rep["out_err"] = float(np.max(np.abs(o - ref_out), initial=0.0))
+    rep["out_ref_max"] = ref_max
+    rel, ab = (OUT_REL_BF16, OUT_ABS_BF16) if kv_format == "bf16" else (OUT_REL_FP8, OUT_ABS_FP8)
+    rep["out_bound"] = rel * ref_max + ab
+    ok &= rep["out_err"] <= rep["out_bound"]
+    ok &= bool(np.all(np.isfinite(o)))
+    return ok, rep

@@ -1,0 +1,60 @@
+"""The C-ABI library builds for sm_103a, loads without a GPU and exports every
+symbol include/dsa.h declares; host-side validation answers without a device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from sparse_mla_attention_dsa_gb300 import _lib, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return _lib.load()
+
+
+def _declared_symbols():
+    text = open(os.path.join(ROOT, "include", "dsa.h")).read()
+    return sorted(set(re.findall(r"DSA_API\s+[\w\s\*]+?\b(dsa_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    names = _declared_symbols()
+    assert {"dsa_sparse_attn_fwd", "dsa_sparse_attn_fwd_fp8kv", "dsa_sparse_attn_fwd_workspace_size",
+            "dsa_read_device_status", "dsa_status_string", "dsa_kernels_per_call"} <= set(names)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared_symbols():
+        assert hasattr(lib, name), name
+    assert set(_declared_symbols()) == set(_lib.SIGNATURES)
+
+
+def test_status_strings(lib):
+    for code, name in _lib.STATUS.items():
+        assert lib.dsa_status_string(code).decode() == name
+    assert lib.dsa_status_string(99).decode() == "DSA_ERR_UNKNOWN"
+    assert lib.dsa_kernels_per_call() == 3
+
+
+def test_host_validation_needs_no_device(lib):
+    f = lib.dsa_sparse_attn_fwd
+    null = ctypes.c_void_p(0)
+    args = lambda s_q, h_q, s_kv, topk, scale=0.1: (null, null, null, s_q, h_q, s_kv, topk, ctypes.c_float(scale),
+                                                    null, null, null, ctypes.c_size_t(0), null)
+    assert f(*args(0, 16, 10, 4)) == 0               # nothing to do
+    assert f(*args(-1, 16, 10, 4)) == 1              # negative s_q
+    assert f(*args(2, 0, 10, 4)) == 1                # h_q out of range
+    assert f(*args(2, 129, 10, 4)) == 1
+    assert f(*args(2, 16, -1, 4)) == 1
+    assert f(*args(2, 16, 10, 0)) == 1               # topk < 1
+    assert f(*args(2, 16, 10, 4, float("nan"))) == 1
+    assert f(*args(2, 16, 10, 4)) == 1               # null data pointers
+    bad = ctypes.c_void_p(0x1008)                     # 8-byte aligned only
+    assert f(bad, bad, bad, 2, 16, 10, 4, ctypes.c_float(0.1), bad, bad, bad, ctypes.c_size_t(0), null) == 3
+    assert lib.dsa_sparse_attn_fwd_workspace_size(-1, 16, 4, 0) == 0
+    assert lib.dsa_sparse_attn_fwd_workspace_size(4, 16, 4, 7) == 0
