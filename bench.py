@@ -1,0 +1,314 @@
+#!/usr/bin/env python3
+"""Benchmark of the sparse MLA (DeepSeek Sparse Attention) forward on GB300.
+
+Workload: causal prefill, 4096 query tokens x 128 heads over s_kv = 8192 latent
+rows, topk = 2048 indices per token of which 102 are -1 (n_valid = 1946),
+Q/KV ~ N(0,1) bf16, sm_scale = 1/sqrt(576).  One step = one forward call over
+the whole batch (counting/scheduling kernel, attention kernel, split-token merge).
+
+Prints ONE JSON line (rank 0).  FLOPs per token = 2 * h_q * n_valid * (576 + 512);
+``value`` is whole-job TFLOP/s with inputs resident in HBM; ``e2e`` is the same
+metric through the public API with pinned host buffers (H2D of the inputs and
+D2H of out/lse inside every timed step); ``roofline`` is the attention kernel
+alone (CUDA events recorded around it inside the library call) against the
+measured dense bf16 tensor peak; ``cpu_baseline`` is the float64 CPU oracle on a
+time-bounded sample of the same tokens.
+
+``--impl reference`` times that CPU oracle (the only reference implementation
+of this path) on the host cores instead, each step a bounded sample of tokens.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+METRIC = "sparse MLA fwd TFLOPS & % of roofline (h_q=128, topk=2048, 1×GB300)"
+UNIT = "TFLOP/s"
+WORKLOAD = "prefill_causal"
+L2_FLUSH_BYTES = 2 * 135_528_448  # twice the GB300 L2
+
+
+def _flops(indices: torch.Tensor, s_kv: int, h_q: int) -> float:
+    nv = ((indices >= 0) & (indices < s_kv)).sum().item()
+    return 2.0 * h_q * nv * (576 + 512)
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops"]), float(d["hbm_gbs"]), "measured (MEASURED_PEAKS.json, bf16 burst)"
+    return 1900.0, 6800.0, "fallback (1.9 PFLOP/s bf16, 6.8 TB/s)"
+
+
+class ClockSampler:
+    """nvidia-smi samples every 200 ms while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "200", "-i", str(gpu_index)], stdout=self.f,
+                                         stderr=subprocess.DEVNULL)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.flush()
+        self.f.seek(0)
+        rows = [r.split(",") for r in self.f.read().strip().splitlines() if r.count(",") >= 8]
+        os.unlink(self.f.name)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].strip().replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].strip().replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].strip() == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def cpu_oracle_sample(wl, seconds: float, start_token: int = 0):
+    """Run the float64 oracle token by token for about `seconds`; returns (flops, elapsed, n_tokens)."""
+    from oracle import dsa_oracle as O
+    qb = wl.q.contiguous().view(torch.int16).numpy().view(np.uint16)
+    kvr = wl.kv.contiguous().view(torch.int16).numpy().view(np.uint16)
+    idx = wl.indices.numpy()
+    flops, n, t0 = 0.0, 0, time.perf_counter()
+    t = start_token
+    while True:
+        O.sparse_mla_fwd_sampled(qb, kvr, "bf16", idx, wl.sm_scale, [t % wl.s_q])
+        row = idx[t % wl.s_q]
+        flops += 2.0 * wl.h_q * int(((row >= 0) & (row < wl.s_kv)).sum()) * 1088
+        n += 1
+        t += 1
+        if time.perf_counter() - t0 >= seconds or n >= wl.s_q:
+            break
+    return flops, time.perf_counter() - t0, n
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def run_reference(args, rank: int, world: int):
+    """The CPU oracle as it stands, on this host's cores, each step a bounded token sample."""
+    from sparse_mla_attention_dsa_gb300 import workloads as W
+    if rank != 0:
+        return
+    wl = W.prefill_causal()
+    for w in range(args.warmup):
+        cpu_oracle_sample(wl, 0.0, start_token=w)
+    times, flops_all, ntok = [], 0.0, 0
+    tok = args.warmup
+    for _ in range(args.steps):
+        f, dt, n = cpu_oracle_sample(wl, args.ref_step_seconds, start_token=tok)
+        tok += n
+        times.append(dt)
+        flops_all += f
+        ntok += n
+    total = sum(times)
+    value = flops_all / total / 1e12
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+            "config": {"workload": WORKLOAD, "s_q": wl.s_q, "h_q": wl.h_q, "s_kv": wl.s_kv, "topk": wl.topk,
+                       "n_valid_per_token": 1946, "step": f"~{args.ref_step_seconds:g} s token sample"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": host_cores(), "kind": "oracle",
+                             "sample": f"{ntok} tokens of {WORKLOAD} over {args.steps} steps (numpy float64, "
+                                       f"BLAS threads = host cores)"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_gb300(args, rank: int, world: int, local_rank: int):
+    from sparse_mla_attention_dsa_gb300 import api, build
+    from sparse_mla_attention_dsa_gb300 import workloads as W
+    build.build()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    wl = W.prefill_causal(seed=2 + rank, s_q=args.s_q, s_kv=args.s_q + 4096)
+    flops = _flops(wl.indices, wl.s_kv, wl.h_q)
+    q, kv, idx = wl.q.to(dev), wl.kv.to(dev), wl.indices.to(dev)
+    out = torch.empty((wl.s_q, wl.h_q, 512), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((wl.s_q, wl.h_q), dtype=torch.float32, device=dev)
+    ws = torch.empty(api.dsa_sparse_attn_fwd_workspace_size(wl.s_q, wl.h_q, wl.topk), dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        api.dsa_sparse_attn_fwd(q, kv, idx, wl.sm_scale, out=out, lse=lse, workspace=ws)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    api.dsa_read_device_status(ws)
+    torch.cuda.synchronize()
+
+    # ---- device-resident timed region (per-step events; L2 flushed between steps, outside the events)
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    for a, b in kev:  # materialise the events before handing them to the library
+        a.record(stream)
+        b.record(stream)
+    sampler = ClockSampler(local_rank)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    for i in range(K):
+        flush.zero_()
+        api.dsa_set_timing_events(kev[i][0], kev[i][1])
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    api.dsa_set_timing_events()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop()
+    api.dsa_read_device_status(ws)
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    kern_ms = [a.elapsed_time(b) for a, b in kev]
+    ms = sum(step_ms) / K
+    kms = sum(kern_ms) / K
+    if world > 1:
+        t = torch.tensor([ms, kms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms, kms = float(t[0]), float(t[1])
+
+    # ---- end to end through the public API from pinned host buffers
+    e2e_ms = float('nan')
+    if not args.skip_e2e:
+        e2e_ms = _e2e(args, wl, q, kv, idx, out, lse, step, stream, world, dev)
+
+    if rank != 0:
+        return
+    return _report(args, wl, flops, ms, kms, e2e_ms, clocks, world)
+
+
+def _e2e(args, wl, q, kv, idx, out, lse, step, stream, world, dev):
+    qh, kvh, idxh = wl.q.pin_memory(), wl.kv.pin_memory(), wl.indices.pin_memory()
+    outh = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    lseh = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+
+    def e2e_step():
+        q.copy_(qh, non_blocking=True)
+        kv.copy_(kvh, non_blocking=True)
+        idx.copy_(idxh, non_blocking=True)
+        step()
+        outh.copy_(out, non_blocking=True)
+        lseh.copy_(lse, non_blocking=True)
+
+    for _ in range(max(2, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize()
+    KE = max(3, min(args.steps, 10))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(KE):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / KE
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t[0])
+
+    return e2e_ms
+
+
+def _report(args, wl, flops, ms, kms, e2e_ms, clocks, world):
+    from sparse_mla_attention_dsa_gb300 import api
+    K = args.steps
+    h2d = wl.q.numel() * 2 + wl.kv.numel() * 2 + wl.indices.numel() * 4
+    d2h = wl.s_q * wl.h_q * (512 * 2 + 4)
+    peak_tf, hbm_gbs, peak_src = _peaks()
+    achieved = flops / (kms * 1e-3) / 1e12
+    value = world * flops / (ms * 1e-3) / 1e12
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
+            "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": WORKLOAD, "s_q": wl.s_q, "h_q": wl.h_q, "s_kv": wl.s_kv, "topk": wl.topk,
+                       "n_valid_per_token": 1946, "b_topk": 64, "kv": "bf16", "seed": 2,
+                       "l2": "flushed before every step (270 MB write, outside the step events)",
+                       "parallelism": f"replicas x{world} (tokens are independent)"},
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s",
+                         "frac": achieved / peak_tf, "traffic": args.traffic, "peak_source": peak_src,
+                         "kernel": "dsa_fwd_bf16_kernel", "kernel_ms": kms},
+            "e2e": None if args.skip_e2e else {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+                                               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                                               "ms_per_step": e2e_ms},
+            "gpu_launches": K * api.dsa_kernels_per_call(),
+            "clocks": clocks}
+    if not args.no_cpu_baseline:
+        f, dt, n = cpu_oracle_sample(wl, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": f / dt / 1e12, "unit": UNIT, "cores": host_cores(), "kind": "oracle",
+                                "sample": f"{n} tokens of {WORKLOAD} ({dt:.1f} s, numpy float64, "
+                                          f"BLAS threads = host cores)"}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--ref-step-seconds", type=float, default=2.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--s-q", type=int, default=4096, help="query tokens (4096 = the benchmark workload)")
+    ap.add_argument("--skip-e2e", action="store_true")
+    ap.add_argument("--traffic", type=float, default=None,
+                    help="DRAM bytes per attention-kernel launch from an ncu capture (null when not given)")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if world > 1:
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl")
+    try:
+        run_gb300(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -10,7 +10,7 @@
  *     out_t    = S @ gathered[:, :512]                       [h_q, 512]
  *     lse_t    = ln(sum(exp(sm_scale * Q_t @ gathered^T)))   [h_q]
  *
- * computed blockwise over index blocks of 64 with the online softmax of section
+ * computed blockwise over index blocks of 128 with the online softmax of section
  * "计算流程": float32 running max / max-for-softmax / sum-of-exp, a float32
  * output accumulator, a rescale that fires only when the running max has moved
  * more than 6 (natural-log units) above the max used for the exponentials
@@ -63,7 +63,7 @@ extern "C" {
 #define DSA_D_ROPE 64
 #define DSA_FP8_ROW_BYTES 656
 #define DSA_MAX_HEADS 128
-#define DSA_B_TOPK 64
+#define DSA_B_TOPK 128
 
 typedef enum {
   DSA_OK = 0,
@@ -117,6 +117,14 @@ DSA_API const char* dsa_status_string(dsa_status status);
 
 /* Number of kernels one forward call launches (the memset excluded). */
 DSA_API int dsa_kernels_per_call(void);
+
+/* Profiling hook.  When both events are non-null, every later forward call
+ * records `before` on its stream just before the attention kernel and `after`
+ * just after it, so a caller can time that kernel alone with
+ * cudaEventElapsedTime.  Pass two nulls to switch it off.  The events are
+ * created and owned by the caller; the setting is process-wide and not
+ * thread-safe (meant for benchmarks). */
+DSA_API void dsa_set_timing_events(cudaEvent_t before, cudaEvent_t after);
 
 #ifdef __cplusplus
 }

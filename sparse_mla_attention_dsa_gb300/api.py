@@ -100,3 +100,15 @@ def dsa_status_string(code: int) -> str:
 
 def dsa_kernels_per_call() -> int:
     return int(_lib.load().dsa_kernels_per_call())
+
+
+def dsa_set_timing_events(before=None, after=None) -> None:
+    """Have later forward calls record two torch.cuda.Event objects around the attention kernel.
+
+    Both events must already exist on the device (record them once first); pass
+    no arguments to switch the hook off.
+    """
+    if before is None or after is None:
+        _lib.load().dsa_set_timing_events(ctypes.c_void_p(0), ctypes.c_void_p(0))
+        return
+    _lib.load().dsa_set_timing_events(ctypes.c_void_p(before.cuda_event), ctypes.c_void_p(after.cuda_event))

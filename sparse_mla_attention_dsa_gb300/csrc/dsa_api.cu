@@ -1,8 +1,6 @@
 // C ABI of the sparse MLA forward (see include/dsa.h), the scheduling kernel
 // that counts valid index slots and lays out the work sequence, and the kernel
 // that merges the pieces of tokens split across CTA pairs.
-#include <cuda.h>
-#include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -15,7 +13,7 @@
 namespace dsa {
 
 int fwd_max_active_pairs();
-cudaError_t launch_fwd_bf16(const CUtensorMap& tmap, const FwdParams& p, cudaStream_t stream);
+cudaError_t launch_fwd_bf16(const FwdParams& p, cudaStream_t stream);
 int fwd_fp8_max_active_pairs();
 cudaError_t launch_fwd_fp8(const FwdParams& p, cudaStream_t stream);
 
@@ -156,19 +154,6 @@ __global__ void dsa_fill_empty_kernel(uint16_t* out, float* lse, size_t n_out, s
   for (size_t k = i; k < n_lse; k += stride) lse[k] = -INFINITY;
 }
 
-static PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
-    cudaDriverEntryPointQueryResult q;
-    void* f = nullptr;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = (PFN_cuTensorMapEncodeTiled_v12000)f;
-  }
-  return fn;
-}
-
 static bool device_ok() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return false;
@@ -183,6 +168,8 @@ static int pairs_for(int kv_format) {
 }
 
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+static cudaEvent_t g_ev_before = nullptr, g_ev_after = nullptr;
 
 static dsa_status forward(int kv_format, const void* q, const void* kv, const int32_t* indices, int s_q, int h_q,
                           int s_kv, int topk, float sm_scale, void* out, float* lse, void* workspace,
@@ -230,22 +217,10 @@ static dsa_status forward(int kv_format, const void* q, const void* kv, const in
   if (cudaGetLastError() != cudaSuccess) return DSA_ERR_CUDA;
 
   cudaError_t e;
-  if (kv_format == DSA_KV_BF16) {
-    auto encode = get_encode_fn();
-    if (!encode) return DSA_ERR_UNSUPPORTED;
-    CUtensorMap tmap;
-    cuuint64_t dims[2] = {(cuuint64_t)kDQK, (cuuint64_t)s_kv};
-    cuuint64_t strides[1] = {(cuuint64_t)kDQK * 2};
-    cuuint32_t box[2] = {64, 1};
-    cuuint32_t estr[2] = {1, 1};
-    CUresult cr = encode(&tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(kv), dims, strides, box, estr,
-                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (cr != CUDA_SUCCESS) return DSA_ERR_CUDA;
-    e = launch_fwd_bf16(tmap, p, stream);
-  } else {
-    e = launch_fwd_fp8(p, stream);
-  }
+  const bool timed = g_ev_before != nullptr && g_ev_after != nullptr;
+  if (timed) cudaEventRecord(g_ev_before, stream);
+  e = (kv_format == DSA_KV_BF16) ? launch_fwd_bf16(p, stream) : launch_fwd_fp8(p, stream);
+  if (timed) cudaEventRecord(g_ev_after, stream);
   if (e != cudaSuccess) return DSA_ERR_CUDA;
   dsa_combine_kernel<<<npairs, 256, 0, stream>>>(p.cum, p.ctrl, s_q, h_q, npairs, p.part_lse, p.part_o,
                                                  (uint16_t*)out, lse);
@@ -300,5 +275,10 @@ const char* dsa_status_string(dsa_status s) {
 }
 
 int dsa_kernels_per_call(void) { return 3; }
+
+void dsa_set_timing_events(cudaEvent_t before, cudaEvent_t after) {
+  dsa::g_ev_before = before;
+  dsa::g_ev_after = after;
+}
 
 }  // extern "C"

@@ -9,7 +9,7 @@ namespace dsa {
 
 constexpr int kDQK = 576;        // latent 512 + rope 64
 constexpr int kDV = 512;         // output channels (first 512 KV columns)
-constexpr int kBT = 64;          // B_TOPK: index block processed per step
+constexpr int kBT = 128;         // B_TOPK: index block processed per step
 constexpr int kMaxHeads = 128;   // the MMA M dimension; smaller h_q is padded
 constexpr int kFp8RowBytes = 656;
 
