@@ -34,17 +34,9 @@ from __future__ import annotations
 
 import numpy as np
 
-from .formats import bf16_bits_to_f64
+from .formats import round_to_bf16  # noqa: F401  (re-exported for tests)
 
 D_V = 512
-
-
-def round_to_bf16(x: np.ndarray) -> np.ndarray:
-    """Round float32 values to the nearest bf16 (ties to even), returned as float32."""
-    x = np.ascontiguousarray(x, dtype=np.float32)
-    b = x.view(np.uint32).astype(np.uint64)
-    rounded = (b + 0x7FFF + ((b >> 16) & 1)) >> 16
-    return bf16_bits_to_f64(rounded.astype(np.uint16)).astype(np.float32)
 
 
 def blockwise_token(q32: np.ndarray, kv32: np.ndarray, idx: np.ndarray, sm_scale: float, b_topk: int = 64,

@@ -10,6 +10,12 @@ FP8 KV row (656 bytes, data and scale adjacent per token, as asked for by
 "Decoding KV Cache Layout 优化"): 512 e4m3 latent codes, 4 float32 scales (one
 per 128 latent channels), 64 bf16 rope values.  Group size and rope dtype are
 this library's reading; the page only fixes that data and scale sit together.
+
+Dequantisation: the same page, section "能不能用 1C1V", has decoding turn the
+FP8 cache into bfloat16 before the matrix unit.  A dequantised latent channel
+is therefore bf16 (round to nearest even) of the float32 product e4m3 * scale:
+the rounding is part of the method's input to the attention, taken in float32
+as the kernel takes it.
 """
 from __future__ import annotations
 
@@ -25,6 +31,14 @@ def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
     """Decode raw bf16 bit patterns (uint16/int16 array) exactly to float64."""
     u32 = bits.astype(np.uint16).astype(np.uint32) << np.uint32(16)
     return u32.view(np.float32).astype(np.float64)
+
+
+def round_to_bf16(x: np.ndarray) -> np.ndarray:
+    """Round float32 values to the nearest bf16 (ties to even), returned as float32."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    b = x.view(np.uint32).astype(np.uint64)
+    rounded = (b + 0x7FFF + ((b >> 16) & 1)) >> 16
+    return bf16_bits_to_f64(rounded.astype(np.uint16)).astype(np.float32)
 
 
 def e4m3_to_f64(codes: np.ndarray) -> np.ndarray:
@@ -43,14 +57,14 @@ def e4m3_to_f64(codes: np.ndarray) -> np.ndarray:
 def fp8_rows_to_f64(rows: np.ndarray) -> np.ndarray:
     """Dequantise 656-byte FP8 KV rows [n, 656] (uint8) to float64 [n, 576].
 
-    latent[c] = e4m3(code[c]) * scale[c // 128] (exact in float64);
+    latent[c] = bf16(float32(e4m3(code[c]) * scale[c // 128])) (see the module note);
     rope = the bf16 values as stored.
     """
     rows = np.ascontiguousarray(rows, dtype=np.uint8)
     n = rows.shape[0]
-    lat = e4m3_to_f64(rows[:, :D_V])
-    scale = rows[:, D_V:D_V + 16].copy().view(np.float32).astype(np.float64)  # [n, 4]
-    lat = lat * np.repeat(scale, FP8_GROUP, axis=1)
+    lat = e4m3_to_f64(rows[:, :D_V]).astype(np.float32)  # e4m3 values are exact in float32
+    scale = rows[:, D_V:D_V + 16].copy().view(np.float32)  # [n, 4]
+    lat = round_to_bf16(lat * np.repeat(scale, FP8_GROUP, axis=1)).astype(np.float64)
     rope = bf16_bits_to_f64(rows[:, D_V + 16:].copy().view(np.uint16))
     out = np.empty((n, D_V + D_ROPE), dtype=np.float64)
     out[:, :D_V] = lat
