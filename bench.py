@@ -11,8 +11,10 @@ Prints ONE JSON line (rank 0).  FLOPs per token = 2 * h_q * n_valid * (576 + 512
 metric through the public API with pinned host buffers (H2D of the inputs and
 D2H of out/lse inside every timed step); ``roofline`` is the attention kernel
 alone (CUDA events recorded around it inside the library call) against the
-measured dense bf16 tensor peak; ``cpu_baseline`` is the float64 CPU oracle on a
-time-bounded sample of the same tokens.
+bound that dominates max(FLOPs / bf16 peak, algorithmic bytes / HBM peak), the
+algorithmic bytes being the gathered KV rows plus Q, out, lse and indices;
+``cpu_baseline`` is the float64 CPU oracle on a time-bounded sample of the same
+tokens.  ``--workload`` selects one of the other input shapes for measurement.
 
 ``--impl reference`` times that CPU oracle (the only reference implementation
 of this path) on the host cores instead, each step a bounded sample of tokens.
@@ -43,6 +45,13 @@ L2_FLUSH_BYTES = 2 * 135_528_448  # twice the GB300 L2
 def _flops(indices: torch.Tensor, s_kv: int, h_q: int) -> float:
     nv = ((indices >= 0) & (indices < s_kv)).sum().item()
     return 2.0 * h_q * nv * (576 + 512)
+
+
+def _alg_bytes(wl) -> float:
+    """Algorithmic bytes of one forward: gathered KV rows + Q + out + lse + indices."""
+    nv = ((wl.indices >= 0) & (wl.indices < wl.s_kv)).sum().item()
+    row = 1152 if wl.kv_format == "bf16" else 656
+    return nv * row + wl.s_q * wl.h_q * (576 * 2 + 512 * 2 + 4) + wl.indices.numel() * 4
 
 
 def _peaks():
@@ -97,12 +106,12 @@ def cpu_oracle_sample(wl, seconds: float, start_token: int = 0):
     """Run the float64 oracle token by token for about `seconds`; returns (flops, elapsed, n_tokens)."""
     from oracle import dsa_oracle as O
     qb = wl.q.contiguous().view(torch.int16).numpy().view(np.uint16)
-    kvr = wl.kv.contiguous().view(torch.int16).numpy().view(np.uint16)
+    kvr = wl.kv.contiguous().view(torch.int16).numpy().view(np.uint16) if wl.kv_format == "bf16" else wl.kv.numpy()
     idx = wl.indices.numpy()
     flops, n, t0 = 0.0, 0, time.perf_counter()
     t = start_token
     while True:
-        O.sparse_mla_fwd_sampled(qb, kvr, "bf16", idx, wl.sm_scale, [t % wl.s_q])
+        O.sparse_mla_fwd_sampled(qb, kvr, wl.kv_format, idx, wl.sm_scale, [t % wl.s_q])
         row = idx[t % wl.s_q]
         flops += 2.0 * wl.h_q * int(((row >= 0) & (row < wl.s_kv)).sum()) * 1088
         n += 1
@@ -155,17 +164,22 @@ def run_gb300(args, rank: int, world: int, local_rank: int):
     build.build()
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
-    wl = W.prefill_causal(seed=2 + rank, s_q=args.s_q, s_kv=args.s_q + 4096)
+    if args.workload == "prefill_causal":
+        wl = W.prefill_causal(seed=2 + rank, s_q=args.s_q, s_kv=args.s_q + 4096)
+    else:
+        wl = W.WORKLOADS[args.workload]()
     flops = _flops(wl.indices, wl.s_kv, wl.h_q)
+    fwd = api.dsa_sparse_attn_fwd if wl.kv_format == "bf16" else api.dsa_sparse_attn_fwd_fp8kv
     q, kv, idx = wl.q.to(dev), wl.kv.to(dev), wl.indices.to(dev)
     out = torch.empty((wl.s_q, wl.h_q, 512), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((wl.s_q, wl.h_q), dtype=torch.float32, device=dev)
-    ws = torch.empty(api.dsa_sparse_attn_fwd_workspace_size(wl.s_q, wl.h_q, wl.topk), dtype=torch.uint8, device=dev)
+    ws = torch.empty(api.dsa_sparse_attn_fwd_workspace_size(wl.s_q, wl.h_q, wl.topk, 0 if wl.kv_format == "bf16" else 1),
+                     dtype=torch.uint8, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
     def step():
-        api.dsa_sparse_attn_fwd(q, kv, idx, wl.sm_scale, out=out, lse=lse, workspace=ws)
+        fwd(q, kv, idx, wl.sm_scale, out=out, lse=lse, workspace=ws)
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -250,21 +264,33 @@ def _e2e(args, wl, q, kv, idx, out, lse, step, stream, world, dev):
 def _report(args, wl, flops, ms, kms, e2e_ms, clocks, world):
     from sparse_mla_attention_dsa_gb300 import api
     K = args.steps
-    h2d = wl.q.numel() * 2 + wl.kv.numel() * 2 + wl.indices.numel() * 4
+    h2d = wl.q.numel() * 2 + wl.kv.numel() * wl.kv.element_size() + wl.indices.numel() * 4
     d2h = wl.s_q * wl.h_q * (512 * 2 + 4)
     peak_tf, hbm_gbs, peak_src = _peaks()
-    achieved = flops / (kms * 1e-3) / 1e12
+    abytes = _alg_bytes(wl)
+    t_flops, t_bytes = flops / (peak_tf * 1e12), abytes / (hbm_gbs * 1e9)
+    tf_achieved = flops / (kms * 1e-3) / 1e12
+    gbs_achieved = abytes / (kms * 1e-3) / 1e9
+    if t_bytes >= t_flops:
+        roof = {"bound": "hbm", "achieved": gbs_achieved, "peak": hbm_gbs, "unit": "GB/s",
+                "frac": gbs_achieved / hbm_gbs}
+    else:
+        roof = {"bound": "tensor", "achieved": tf_achieved, "peak": peak_tf, "unit": "TFLOP/s",
+                "frac": tf_achieved / peak_tf}
+    roof.update({"traffic": args.traffic, "alg_bytes": abytes, "alg_flops": flops, "peak_source": peak_src,
+                 "kernel": "dsa_fwd_kernel<%s>" % ("false" if wl.kv_format == "bf16" else "true"),
+                 "kernel_ms": kms, "tensor_frac": tf_achieved / peak_tf, "hbm_frac": gbs_achieved / hbm_gbs,
+                 "roofline_ms": 1e3 * max(t_flops, t_bytes)})
     value = world * flops / (ms * 1e-3) / 1e12
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
             "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic",
-            "config": {"workload": WORKLOAD, "s_q": wl.s_q, "h_q": wl.h_q, "s_kv": wl.s_kv, "topk": wl.topk,
-                       "n_valid_per_token": 1946, "b_topk": 64, "kv": "bf16", "seed": 2,
+            "config": {"workload": args.workload, "s_q": wl.s_q, "h_q": wl.h_q, "s_kv": wl.s_kv, "topk": wl.topk,
+                       "n_valid_per_token": round(flops / (2 * wl.h_q * 1088 * wl.s_q), 1), "b_topk": 128,
+                       "kv": wl.kv_format,
                        "l2": "flushed before every step (270 MB write, outside the step events)",
                        "parallelism": f"replicas x{world} (tokens are independent)"},
-            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s",
-                         "frac": achieved / peak_tf, "traffic": args.traffic, "peak_source": peak_src,
-                         "kernel": "dsa_fwd_bf16_kernel", "kernel_ms": kms},
+            "roofline": roof,
             "e2e": None if args.skip_e2e else {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
                                                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                                                "ms_per_step": e2e_ms},
@@ -273,7 +299,7 @@ def _report(args, wl, flops, ms, kms, e2e_ms, clocks, world):
     if not args.no_cpu_baseline:
         f, dt, n = cpu_oracle_sample(wl, args.cpu_seconds)
         line["cpu_baseline"] = {"value": f / dt / 1e12, "unit": UNIT, "cores": host_cores(), "kind": "oracle",
-                                "sample": f"{n} tokens of {WORKLOAD} ({dt:.1f} s, numpy float64, "
+                                "sample": f"{n} tokens of {args.workload} ({dt:.1f} s, numpy float64, "
                                           f"BLAS threads = host cores)"}
     print(json.dumps(line), flush=True)
 
@@ -289,6 +315,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--s-q", type=int, default=4096, help="query tokens (4096 = the benchmark workload)")
     ap.add_argument("--skip-e2e", action="store_true")
+    ap.add_argument("--workload", default="prefill_causal",
+                    choices=["prefill_causal", "decode_bf16", "decode_fp8", "long_prefill", "tiny"])
     ap.add_argument("--traffic", type=float, default=None,
                     help="DRAM bytes per attention-kernel launch from an ncu capture (null when not given)")
     args = ap.parse_args()

@@ -1,11 +1,8 @@
-// FP8-KV variant of the forward (656-byte rows).  Placeholder until the
-// dequantising kernel lands: reports no capacity, so the API returns
-// DSA_ERR_UNSUPPORTED for the FP8 entry point.
-#include <cuda_runtime.h>
-
-#include "dsa_internal.h"
+// FP8-KV instantiation of the sparse MLA forward (see dsa_fwd_impl.cuh): 656-byte
+// rows of 512 e4m3 latent codes, 4 fp32 scales and 64 bf16 rope values.
+#include "dsa_fwd_impl.cuh"
 
 namespace dsa {
-int fwd_fp8_max_active_pairs() { return 0; }
-cudaError_t launch_fwd_fp8(const FwdParams&, cudaStream_t) { return cudaErrorNotSupported; }
+int fwd_fp8_max_active_pairs() { return max_active_pairs_impl<true>(); }
+cudaError_t launch_fwd_fp8(const FwdParams& p, cudaStream_t stream) { return launch_impl<true>(p, stream); }
 }  // namespace dsa

@@ -1,0 +1,980 @@
+// The sparse MLA forward kernel for sm_103a, templated on the KV format
+// (bf16 rows of 576 values, or FP8 rows of 512 e4m3 + 4 fp32 scales + 64 bf16).
+//
+// Method: "Ascend Sparse Attention Forward 算法与优化技术简析", sections
+// "数学建模" (what is computed) and "计算流程" (blockwise online softmax with
+// skip-scale).  The page's delayed P@V order (section "流水线") survives as
+// a pipeline across two SMs; its index prefetch / multi-stage gather idea
+// survives as chunk rings fed by cp.async; its FP8 decoding (section
+// "能不能用 1C1V": KV dequantised to bf16 before the matrix unit) is done by
+// the gather warps on their way into the swizzled operand layouts.
+//
+// Mapping onto a GB300 SM pair (one 2-CTA cluster per unit of work):
+//   * 128 heads x 512 fp32 output columns fill one SM's whole tensor memory,
+//     and all 128 heads x 576 Q columns must sit beside the logits of any SM
+//     that forms them, so the two jobs go to different SMs:
+//       CTA 0 ("QK side") holds Q in tensor memory (latent 512 columns as the
+//       MMA A operand, rope 64 columns in shared memory), computes the logits
+//       of each 128-index block into one of two TMEM tiles, runs the online
+//       softmax with skip-scale on 8 warps and sends the bf16 P tile plus the
+//       per-row rescale factors to its peer with one bulk DSMEM copy.
+//       CTA 1 ("PV side") holds O[128, 512] in tensor memory, applies the
+//       rescale factors, multiplies P by V and writes the normalised output.
+//     Tensor work per block is 576 vs 512 column-units, so the pair is
+//     balanced; only bf16 P crosses between the SMs (one way).
+//   * Gathers use cp.async (16 bytes per thread) with the address swizzled on
+//     the way in, straight into the 128-byte-swizzled layouts tcgen05.mma
+//     reads: 16 KB chunks of 128 rows x 64 columns (K-major) on the QK side,
+//     16 KB row groups of 16 rows x 512 columns (MN-major) on the PV side.
+//     FP8 rows are first staged raw in a small ring, then dequantised.
+//   * Work: the index blocks of all tokens form one sequence; pair p takes the
+//     contiguous range [p*T/P, (p+1)*T/P).  A token cut by a range boundary is
+//     written as normalised partials and merged by the combine kernel.
+//
+// Warp roles (512 threads, both CTAs): warp 0 compacts the valid indices of
+// each block into a small ring of index lists; warp 2 issues tcgen05.mma;
+// warp 3 owns the TMEM allocation (and, on the PV side, returns P slots to
+// the QK side).  QK side: warps 4-11 run the softmax (warp w serves TMEM lane
+// quarter w % 4 and column half (w - 4) / 4), warps 1 and 12-15 gather.  PV
+// side: warps 4-7 rescale O and run the epilogue (one TMEM lane quarter each),
+// warps 1 and 8-15 gather.  Gathering gets many warps because a GB300 SM
+// ingests random 128-byte row pieces at only a few tens of bytes per clock.
+#pragma once
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+
+#include "dsa_internal.h"
+#include "ptx.cuh"
+
+namespace dsa {
+
+namespace fwd {
+
+constexpr int kThreads = 512;
+constexpr int kSoftmaxWarps = 8;                 // QK side, warps 4..11
+constexpr int kEpiWarps = 4;                     // PV side, warps 4..7
+constexpr int kGatherWarpsA = 5;                 // QK side: warps 1, 12..15
+constexpr int kGatherWarpsB = 9;                 // PV side: warps 1, 8..15
+constexpr int kIdxSlots = 4;                     // ring of per-block index lists
+constexpr int kIdxSlotInts = kBT + 4;            // 128 row ids + count
+
+// ---- operand tiles and the P message
+constexpr int kKChunkBytes = 128 * 128;          // 128 rows x 64 bf16 columns, SW128 K-major
+constexpr int kChunksPerBlock = 9;               // 576 / 64
+constexpr int kMsgPBytes = 2 * kKChunkBytes;     // P[128 rows, 128 cols] bf16 = two SW128 chunks
+constexpr int kMsgTrailer = 3 * 128 * 4 + 16;    // alpha[128], inv_se[128], lse[128], flags
+constexpr int kMsgBytes = kMsgPBytes + kMsgTrailer;
+constexpr int kMsgSlot = 34816;                  // 34 KB, 1024-aligned slots
+static_assert(kMsgBytes <= kMsgSlot && kMsgBytes % 16 == 0, "message layout");
+constexpr int kVGroupRows = 16;
+constexpr int kVGroupBytes = kVGroupRows * 1024; // 16 rows x 512 columns bf16 = 8 chunks x 2 KB
+constexpr int kGroupsPerBlock = 128 / kVGroupRows;
+constexpr int kIdxRing = 256;
+constexpr int kMaxKSlots = 8, kMaxVSlots = 9;
+// FP8 rows: raw units staged before dequantisation
+constexpr int kRawSlots = 4;
+constexpr int kRawASlot = 128 * 64;              // QK side unit: 128 rows x 64 bytes (64 e4m3 or 32 bf16)
+constexpr int kRawBRowBytes = 528;               // PV side: first 528 bytes of a row (512 e4m3 + 4 fp32 scales)
+constexpr int kRawBSlot = kVGroupRows * kRawBRowBytes;
+constexpr int kScaleSlot = 128 * 16;             // QK side: 4 fp32 scales of each of 128 rows
+
+__host__ __device__ constexpr int align1k(int x) { return (x + 1023) / 1024 * 1024; }
+
+// Shared-memory layout of each side for one KV format.
+template <bool kFp8>
+struct Lay {
+  static constexpr int kKSlots = kFp8 ? 6 : 8;
+  static constexpr int kVSlots = kFp8 ? 7 : 9;
+  // QK side (cluster rank 0)
+  static constexpr int A_OffK = 0;
+  static constexpr int A_OffRaw = A_OffK + kKSlots * kKChunkBytes;
+  static constexpr int A_OffScales = A_OffRaw + (kFp8 ? kRawSlots * kRawASlot : 0);
+  static constexpr int A_OffQRope = A_OffScales + (kFp8 ? 2 * kScaleSlot : 0);
+  static constexpr int A_OffMsg = align1k(A_OffQRope + kKChunkBytes);
+  static constexpr int A_OffMax = A_OffMsg + 2 * kMsgSlot;  // [2 halves][128] float
+  static constexpr int A_OffSe = A_OffMax + 2 * 128 * 4;
+  static constexpr int A_End = A_OffSe + 2 * 128 * 4;
+  // PV side (cluster rank 1)
+  static constexpr int B_OffV = 0;
+  static constexpr int B_OffRaw = B_OffV + kVSlots * kVGroupBytes;
+  static constexpr int B_OffMsg = align1k(B_OffRaw + (kFp8 ? kRawSlots * kRawBSlot : 0));
+  static constexpr int B_End = B_OffMsg + 2 * kMsgSlot;
+  // common tail: compaction ring, per-block index lists, barriers, misc
+  static constexpr int OffCommon = (A_End > B_End ? A_End : B_End);
+  static constexpr int OffRing = (OffCommon + 127) / 128 * 128;
+  static constexpr int OffIdx = OffRing + kIdxRing * 4;
+  static constexpr int OffBar = OffIdx + kIdxSlots * kIdxSlotInts * 4;
+  static constexpr int NumBars = 56;
+  static constexpr int OffMisc = OffBar + NumBars * 8;
+  static constexpr int SmemUsed = OffMisc + 64;
+  static constexpr int SmemAlloc = SmemUsed + 1024;
+  static_assert(SmemAlloc <= 232448, "shared memory budget");
+};
+
+// barrier slots
+enum BarCommon {
+  IDX_FULL = 0, IDX_EMPTY = IDX_FULL + kIdxSlots, RAW_FULL = IDX_EMPTY + kIdxSlots, RAW_EMPTY = RAW_FULL + kRawSlots,
+  BAR_COMMON_END = RAW_EMPTY + kRawSlots
+};
+enum BarA {
+  A_K_FULL = BAR_COMMON_END, A_K_EMPTY = A_K_FULL + kMaxKSlots, A_S_FULL = A_K_EMPTY + kMaxKSlots,
+  A_S_EMPTY = A_S_FULL + 2, A_Q_FULL = A_S_EMPTY + 2, A_Q_FREE, A_POUT_EMPTY, A_SMX_SYNC = A_POUT_EMPTY + 2, A_DRAIN,
+  A_NUM
+};
+enum BarB {
+  B_V_FULL = BAR_COMMON_END, B_V_EMPTY = B_V_FULL + kMaxVSlots, B_PIN_FULL = B_V_EMPTY + kMaxVSlots,
+  B_RESC_DONE = B_PIN_FULL + 2, B_PV_DONE = B_RESC_DONE + 2, B_O_FULL = B_PV_DONE + 2, B_O_FREE, B_DRAIN, B_NUM
+};
+static_assert((int)A_NUM <= 56 && (int)B_NUM <= 56, "barrier slots");
+
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kTmQ = 0;     // QK side: Q latent [0, 256) (bf16 pairs), S tiles [256, 384) and [384, 512)
+constexpr uint32_t kTmS = 256;
+constexpr uint32_t kIdescQK = idesc_bf16_f32(128, kBT, 0, 0);
+constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 256, 0, 1);
+
+constexpr float kThresLog2 = 6.0f * 1.4426950408889634f;  // RESCALE_THRES = 6 (natural log) in log2 units
+constexpr float kLn2 = 0.6931471805599453f;
+
+// One contiguous run of index blocks of one token.
+struct Piece {
+  int t, lb0, lb1;   // token, first and one-past-last block (within the token)
+  bool full;         // covers all blocks of the token
+  int slot;          // partial-output slot when !full
+};
+
+// Iterates the pieces of pair p's range [p*T/P, (p+1)*T/P) of the global block sequence.
+struct PieceIter {
+  const int* cum;
+  int s_q, g, g1, t, idx, pair;
+  __device__ void init(const int* cum_, int s_q_, int p, int npairs) {
+    cum = cum_;
+    s_q = s_q_;
+    pair = p;
+    const long long T = cum[s_q];
+    g = (int)((long long)p * T / npairs);
+    g1 = (int)((long long)(p + 1) * T / npairs);
+    idx = 0;
+    int lo = 0, hi = s_q - 1;  // largest t with cum[t] <= g
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (cum[mid] <= g) lo = mid; else hi = mid - 1;
+    }
+    t = lo;
+  }
+  __device__ bool next(Piece& pc) {
+    if (g >= g1) return false;
+    const int c0 = cum[t], c1 = cum[t + 1];
+    pc.t = t;
+    pc.lb0 = g - c0;
+    pc.lb1 = min(c1, g1) - c0;
+    pc.full = (pc.lb0 == 0) && (pc.lb1 == c1 - c0);
+    pc.slot = 2 * pair + (idx == 0 ? 0 : 1);
+    g = c0 + pc.lb1;
+    ++t;
+    ++idx;
+    return true;
+  }
+};
+
+__device__ __forceinline__ uint32_t sw128_off(uint32_t row, uint32_t chunk16) {
+  return (row >> 3) * 1024 + (row & 7) * 128 + ((chunk16 ^ (row & 7)) << 4);
+}
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_arrive(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void bulk_s2cluster(uint32_t dst_cluster, uint32_t src_cta, uint32_t bytes,
+                                               uint32_t remote_bar) {
+  asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   dst_cluster),
+               "r"(src_cta), "r"(bytes), "r"(remote_bar)
+               : "memory");
+}
+
+// 16 e4m3 codes (one 16-byte piece, code i in byte i) times `scale`, rounded to
+// bf16: two 16-byte pieces of 8 bf16 each, element order kept.
+__device__ __forceinline__ void dequant16(const uint4 w, float scale, uint4& o0, uint4& o1) {
+  const uint32_t in[4] = {w.x, w.y, w.z, w.w};
+  uint32_t out[8];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const __half2_raw h01 = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(in[i] & 0xFFFFu), __NV_E4M3);
+    const __half2_raw h23 = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(in[i] >> 16), __NV_E4M3);
+    const float2 f01 = __half22float2(__half2(h01));
+    const float2 f23 = __half22float2(__half2(h23));
+    out[2 * i] = pack_bf16x2(f01.x * scale, f01.y * scale);
+    out[2 * i + 1] = pack_bf16x2(f23.x * scale, f23.y * scale);
+  }
+  o0 = make_uint4(out[0], out[1], out[2], out[3]);
+  o1 = make_uint4(out[4], out[5], out[6], out[7]);
+}
+
+struct Ctx {
+  uint8_t* smem;
+  uint32_t sbase, bars, tmem, rank, peer, peer_abort;
+  volatile int* abort_flag;
+  int* status;
+  int warp, lane, pair;
+  __device__ uint32_t bar(int i) const { return bars + 8u * (uint32_t)i; }
+};
+
+__device__ __forceinline__ void set_abort(const Ctx& c) {
+  if (!*c.abort_flag) {
+    *c.abort_flag = 1;
+    atomicCAS(c.status, 0, 5 /* DSA_ERR_DEVICE_TIMEOUT */);
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(c.peer_abort), "r"(1) : "memory");
+  }
+}
+
+__device__ __forceinline__ bool wait(const Ctx& c, int b, uint32_t parity, bool cluster = false) {
+  return mbar_wait(c.bar(b), parity, kWaitLimitNs, c.abort_flag, cluster);
+}
+
+// Bounded barrier among the 8 softmax warps (an mbarrier, so that a warp that
+// gave up cannot leave the others blocked forever).  `n` counts uses.
+__device__ __forceinline__ bool group_sync(const Ctx& c, uint32_t& n) {
+  __syncwarp();
+  if (c.lane == 0) mbar_arrive(c.bar(A_SMX_SYNC));
+  const bool ok = wait(c, A_SMX_SYNC, n & 1u);
+  ++n;
+  return ok;
+}
+
+// Index compaction into a ring: the valid slots of one token, in order.
+struct IndexRing {
+  int* ring;
+  const int32_t* idx_t;
+  int topk, s_kv, head, tail, rp;
+  __device__ void reset(int* r, const int32_t* p, int tk, int skv) {
+    ring = r; idx_t = p; topk = tk; s_kv = skv; head = tail = rp = 0;
+  }
+  // ensure >= kBT entries (or the token's end) are buffered; returns the count for this block
+  __device__ int fill(int lane) {
+    while (tail - head < kBT && rp < topk) {
+      int v[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int i = rp + q * 32 + lane;
+        v[q] = (i < topk) ? __ldg(idx_t + i) : -1;
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const bool ok = (v[q] >= 0) && (v[q] < s_kv);
+        const uint32_t m = __ballot_sync(0xffffffffu, ok);
+        if (ok) ring[(tail + __popc(m & ((1u << lane) - 1u))) & (kIdxRing - 1)] = v[q];
+        tail += __popc(m);
+      }
+      rp += 128;
+      __syncwarp();
+    }
+    return min(kBT, tail - head);
+  }
+  __device__ int at(int i) const { return ring[(head + i) & (kIdxRing - 1)]; }
+  __device__ void pop(int cnt) {
+    head += cnt;
+    __syncwarp();
+  }
+};
+
+__device__ __forceinline__ uint32_t blocks_of_pair(const FwdParams& p, int pair) {
+  PieceIter it;
+  it.init(p.cum, p.s_q, pair, p.npairs);
+  Piece pc;
+  uint32_t n = 0;
+  while (it.next(pc)) n += (uint32_t)(pc.lb1 - pc.lb0);
+  return n;
+}
+
+// ============================================================================ both sides: index lists
+// Warp 0: walks this pair's pieces, compacts the valid slots of each block in
+// order and publishes them (row ids + count) in a ring of kIdxSlots lists.
+template <bool kFp8>
+__device__ void index_compactor(const Ctx& c, const FwdParams& p) {
+  using Y = Lay<kFp8>;
+  IndexRing ir;
+  int* lists = (int*)(c.smem + Y::OffIdx);
+  PieceIter it;
+  it.init(p.cum, p.s_q, c.pair, p.npairs);
+  Piece pc;
+  uint32_t b = 0;
+  bool ok = true;
+  while (ok && it.next(pc)) {
+    ir.reset((int*)(c.smem + Y::OffRing), p.indices + (size_t)pc.t * p.topk, p.topk, p.s_kv);
+    for (int jb = 0; jb < pc.lb1; ++jb) {
+      const int cnt = ir.fill(c.lane);
+      if (jb >= pc.lb0) {
+        const int slot = (int)(b % kIdxSlots);
+        if (!wait(c, IDX_EMPTY + slot, ((b / kIdxSlots) & 1u) ^ 1u)) { ok = false; break; }
+        int* l = lists + slot * kIdxSlotInts;
+#pragma unroll
+        for (int q = 0; q < kBT / 32; ++q) {
+          const int i = q * 32 + c.lane;
+          l[i] = i < cnt ? ir.at(i) : 0;  // padding rows read row 0 and are masked by the softmax
+        }
+        if (c.lane == 0) l[kBT] = cnt;
+        __syncwarp();
+        if (c.lane == 0) mbar_arrive(c.bar(IDX_FULL + slot));
+        ++b;
+      }
+      ir.pop(cnt);
+    }
+  }
+  if (!ok) set_abort(c);
+}
+
+// ============================================================================ QK side
+template <bool kFp8>
+__device__ void qk_gather(const Ctx& c, const FwdParams& p) {
+  using Y = Lay<kFp8>;
+  uint8_t* smem = c.smem;
+  const int warp = c.warp, lane = c.lane;
+  const int gw = (warp == 1) ? 0 : warp - 11;  // 0..4
+  const int gt = gw * 32 + lane;
+  constexpr int kGT = kGatherWarpsA * 32;
+  const int* lists = (const int*)(smem + Y::OffIdx);
+  const uint32_t nblk = blocks_of_pair(p, c.pair);
+  bool ok = true;
+  if constexpr (kFp8) {
+    // Per block 10 raw units of 128 rows x 64 bytes: latent chunks 0..7 (e4m3) and rope halves 8..9
+    // (bf16); the block's scales ride with unit 0.  Units are staged in a 4-slot ring two units ahead,
+    // then dequantised (latent) or copied (rope) into the swizzled K chunk ring.
+    const uint32_t nunits = nblk * 10u;
+    auto issue = [&](uint32_t u) -> bool {
+      const uint32_t b = u / 10u;
+      const int k = (int)(u % 10u), rs = (int)(u % kRawSlots);
+      if (!wait(c, RAW_EMPTY + rs, ((u / kRawSlots) & 1u) ^ 1u)) return false;
+      if (k == 0 && !wait(c, IDX_FULL + (int)(b % kIdxSlots), (b / kIdxSlots) & 1u)) return false;
+      const int* l = lists + (int)(b % kIdxSlots) * kIdxSlotInts;
+      const uint32_t dst = c.sbase + Y::A_OffRaw + (uint32_t)rs * kRawASlot;
+      const int src_off = (k < 8) ? 64 * k : 528 + 64 * (k - 8);
+      for (int q = gt; q < 512; q += kGT)
+        cp_async16(dst + (uint32_t)q * 16u, p.kv + (size_t)l[q >> 2] * kFp8RowBytes + src_off + 16 * (q & 3));
+      if (k == 0) {
+        const uint32_t sd = c.sbase + Y::A_OffScales + (b & 1u) * kScaleSlot;
+        for (int q = gt; q < 128; q += kGT) cp_async16(sd + (uint32_t)q * 16u, p.kv + (size_t)l[q] * kFp8RowBytes + 512);
+      }
+      cp_async_arrive(c.bar(RAW_FULL + rs));
+      return true;
+    };
+    auto consume = [&](uint32_t u) -> bool {
+      const uint32_t b = u / 10u;
+      const int k = (int)(u % 10u), rs = (int)(u % kRawSlots);
+      if (!wait(c, RAW_FULL + rs, (u / kRawSlots) & 1u)) return false;
+      const uint32_t cs = b * (uint32_t)kChunksPerBlock + (uint32_t)min(k, 8);
+      const int s = (int)(cs % Y::kKSlots);
+      if (k <= 8 && !wait(c, A_K_EMPTY + s, ((cs / Y::kKSlots) & 1u) ^ 1u)) return false;
+      const uint8_t* raw = smem + Y::A_OffRaw + rs * kRawASlot;
+      uint8_t* kd = smem + Y::A_OffK + s * kKChunkBytes;
+      if (k < 8) {
+        const float* sc = (const float*)(smem + Y::A_OffScales + (b & 1u) * kScaleSlot);
+        for (int q = gt; q < 512; q += kGT) {
+          const int r = q >> 2, rp = q & 3;
+          uint4 o0, o1;
+          dequant16(*(const uint4*)(raw + q * 16), sc[r * 4 + (k >> 1)], o0, o1);
+          *(uint4*)(kd + sw128_off((uint32_t)r, (uint32_t)(2 * rp))) = o0;
+          *(uint4*)(kd + sw128_off((uint32_t)r, (uint32_t)(2 * rp + 1))) = o1;
+        }
+      } else {
+        for (int q = gt; q < 512; q += kGT)
+          *(uint4*)(kd + sw128_off((uint32_t)(q >> 2), (uint32_t)(4 * (k - 8) + (q & 3)))) = *(const uint4*)(raw + q * 16);
+      }
+      if (k != 8) mbar_arrive(c.bar(A_K_FULL + s));  // chunk 8 (rope) completes with unit 9
+      __syncwarp();
+      if (lane == 0) mbar_arrive(c.bar(RAW_EMPTY + rs));
+      if (k == 9 && lane == 0) mbar_arrive(c.bar(IDX_EMPTY + (int)(b % kIdxSlots)));
+      return true;
+    };
+    for (uint32_t u = 0; u < 2u && u < nunits && ok; ++u) ok = issue(u);
+    for (uint32_t u = 0; u < nunits && ok; ++u) {
+      if (u + 2u < nunits) ok = issue(u + 2u);
+      if (ok) ok = consume(u);
+    }
+    if (!ok) set_abort(c);
+  } else {
+    uint32_t cseq = 0;
+    for (uint32_t b = 0; b < nblk && ok; ++b) {
+      const int slot = (int)(b % kIdxSlots);
+      if (!wait(c, IDX_FULL + slot, (b / kIdxSlots) & 1u)) { ok = false; break; }
+      const int* l = lists + slot * kIdxSlotInts;
+      for (int k = 0; k < kChunksPerBlock; ++k, ++cseq) {
+        const int s = (int)(cseq % Y::kKSlots);
+        if (!wait(c, A_K_EMPTY + s, ((cseq / Y::kKSlots) & 1u) ^ 1u)) { ok = false; break; }
+        const uint32_t dst = c.sbase + Y::A_OffK + (uint32_t)s * kKChunkBytes;
+        for (int q = gt; q < 1024; q += kGT) {
+          const int r = q >> 3, p16 = q & 7;
+          cp_async16(dst + sw128_off((uint32_t)r, (uint32_t)p16), p.kv + (size_t)l[r] * (kDQK * 2) + k * 128 + p16 * 16);
+        }
+        cp_async_arrive(c.bar(A_K_FULL + s));
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(c.bar(IDX_EMPTY + slot));
+    }
+    if (!ok) set_abort(c);
+    // every issued copy lands before the CTA may exit
+    const uint32_t first = cseq > (uint32_t)Y::kKSlots ? cseq - Y::kKSlots : 0u;
+    for (uint32_t q = first; q < cseq; ++q)
+      mbar_wait(c.bar(A_K_FULL + (int)(q % Y::kKSlots)), (q / Y::kKSlots) & 1u, kWaitLimitNs, nullptr);
+  }
+}
+
+template <bool kFp8>
+__device__ void qk_mma(const Ctx& c, const FwdParams& p) {
+  using Y = Lay<kFp8>;
+  if (c.lane == 0) {
+    PieceIter it;
+    it.init(p.cum, p.s_q, c.pair, p.npairs);
+    Piece pc;
+    uint32_t cseq = 0, blk = 0, item = 0;
+    bool ok = true;
+    const uint32_t qrope = c.sbase + Y::A_OffQRope;
+    while (ok && it.next(pc)) {
+      const int nb = pc.lb1 - pc.lb0;
+      if (!wait(c, A_Q_FULL, item & 1u)) { ok = false; break; }
+      for (int j = 0; j < nb && ok; ++j, ++blk) {
+        const int sb = (int)(blk & 1u);
+        if (!wait(c, A_S_EMPTY + sb, ((blk >> 1) & 1u) ^ 1u)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t dS = c.tmem + kTmS + (uint32_t)sb * kBT;
+        for (int k = 0; k < kChunksPerBlock; ++k, ++cseq) {
+          const int s = (int)(cseq % Y::kKSlots);
+          if (!wait(c, A_K_FULL + s, (cseq / Y::kKSlots) & 1u)) { ok = false; break; }
+          fence_proxy_async_smem();  // generic-proxy writes (cp.async / dequant) -> tensor core reads
+          tc_fence_after();
+          const uint32_t chunk = c.sbase + Y::A_OffK + (uint32_t)s * kKChunkBytes;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t bdesc = smem_desc(chunk + (uint32_t)kk * 32u, 16, 1024);
+            const uint32_t acc = (k > 0 || kk > 0) ? 1u : 0u;
+            if (k < 8) mma_ts(dS, c.tmem + kTmQ + (uint32_t)(k * 32 + kk * 8), bdesc, kIdescQK, acc);
+            else mma_ss(dS, smem_desc(qrope + (uint32_t)kk * 32u, 16, 1024), bdesc, kIdescQK, acc);
+          }
+          mma_commit(c.bar(A_K_EMPTY + s));
+        }
+        if (!ok) break;
+        mma_commit(c.bar(A_S_FULL + sb));
+      }
+      mma_commit(c.bar(A_Q_FREE));
+      ++item;
+    }
+    if (!ok) set_abort(c);
+    mma_commit(c.bar(A_DRAIN));
+    mbar_wait(c.bar(A_DRAIN), 0, kWaitLimitNs, nullptr);
+  }
+  __syncwarp();
+}
+
+template <bool kFp8>
+__device__ void qk_softmax(const Ctx& c, const FwdParams& p) {
+  using Y = Lay<kFp8>;
+  uint8_t* smem = c.smem;
+  const int warp = c.warp, lane = c.lane;
+  const int sw = warp - 4;
+  const int quarter = warp & 3, half = sw >> 2;
+  const int r = quarter * 32 + lane;  // head row = TMEM lane
+  const uint32_t trow = c.tmem + ((uint32_t)(quarter * 32) << 16);
+  float* maxbuf = (float*)(smem + Y::A_OffMax);
+  float* sebuf = (float*)(smem + Y::A_OffSe);
+  const uint32_t peer_msg = mapa_shared(c.sbase + Y::B_OffMsg, c.peer);
+  const uint32_t peer_pin_full = mapa_shared(c.bars + 8u * (uint32_t)B_PIN_FULL, c.peer);
+  const float sg = p.scale_log2 < 0.f ? -1.f : 1.f;  // direction the scale preserves
+  PieceIter it;
+  it.init(p.cum, p.s_q, c.pair, p.npairs);
+  Piece pc;
+  uint32_t blk = 0, item = 0, nsync = 0;
+  bool ok = true;
+  while (ok && it.next(pc)) {
+    const int nb = pc.lb1 - pc.lb0;
+    const int nval = p.nvalid[pc.t];
+    // ---- Q for this token: latent columns [256*half, +256) into TMEM, rope (half 0) into smem
+    if (!wait(c, A_Q_FREE, (item & 1u) ^ 1u)) { ok = false; break; }
+    tc_fence_after();
+    {
+      const bool live = r < p.h_q;
+      const uint4* qrow = (const uint4*)(p.q + ((size_t)pc.t * p.h_q + (live ? r : 0)) * kDQK);
+#pragma unroll 1
+      for (int cc = 0; cc < 4; ++cc) {
+        uint32_t v[32];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const uint4 w = live ? __ldg(qrow + half * 32 + cc * 8 + u) : make_uint4(0, 0, 0, 0);
+          v[4 * u] = w.x; v[4 * u + 1] = w.y; v[4 * u + 2] = w.z; v[4 * u + 3] = w.w;
+        }
+        tmem_st32(trow + kTmQ + (uint32_t)(half * 128 + cc * 32), v);
+      }
+      if (half == 0) {
+        uint8_t* qr = smem + Y::A_OffQRope;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const uint4 w = live ? __ldg(qrow + 64 + u) : make_uint4(0, 0, 0, 0);
+          *(uint4*)(qr + sw128_off((uint32_t)r, (uint32_t)u)) = w;
+        }
+        fence_proxy_async_smem();
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(c.bar(A_Q_FULL));
+    }
+    float rm = -INFINITY, rmfs = -INFINITY, se = 0.f;
+    for (int j = 0; j < nb; ++j, ++blk) {
+      const int sb = (int)(blk & 1u);
+      float s[64];
+      if (!wait(c, A_S_FULL + sb, (blk >> 1) & 1u)) { ok = false; break; }
+      tc_fence_after();
+      {
+        uint32_t v[32];
+        tmem_ld32(trow + kTmS + (uint32_t)(sb * kBT + half * 64), v);
+        tmem_wait_ld();
+        reg_fence(v);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) s[i] = __uint_as_float(v[i]);
+        tmem_ld32(trow + kTmS + (uint32_t)(sb * kBT + half * 64 + 32), v);
+        tmem_wait_ld();
+        reg_fence(v);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) s[32 + i] = __uint_as_float(v[i]);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(c.bar(A_S_EMPTY + sb));
+      // ---- row max over both column halves (extreme raw logit in the scale's direction, then scaled)
+      const int nv = min(kBT, max(0, nval - kBT * (pc.lb0 + j)));
+      const int c0 = half * 64;
+      const bool full_blk = (c0 + 64 <= nv);
+      float ext = -INFINITY;
+      if (full_blk) {
+#pragma unroll
+        for (int i = 0; i < 64; ++i) ext = fmaxf(ext, sg * s[i]);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 64; ++i) ext = (c0 + i < nv) ? fmaxf(ext, sg * s[i]) : ext;
+      }
+      const float hmax = (ext == -INFINITY) ? -INFINITY : (sg * ext) * p.scale_log2;
+      maxbuf[half * 128 + r] = hmax;
+      if (!group_sync(c, nsync)) { ok = false; break; }
+      const float cmax = fmaxf(hmax, maxbuf[(half ^ 1) * 128 + r]);
+      rm = fmaxf(rm, cmax);
+      const bool trig = rm > rmfs + kThresLog2;
+      float alpha = 1.f;
+      if (trig) {
+        alpha = ex2_approx(rmfs - rm);
+        se *= alpha;
+        rmfs = rm;
+      }
+      // ---- message slot free?  then exponentials straight into the P tile (this half = one SW128 chunk)
+      const int pb = (int)(blk & 1u);
+      if (!wait(c, A_POUT_EMPTY + pb, ((blk >> 1) & 1u) ^ 1u, true)) { ok = false; break; }
+      uint8_t* msg = smem + Y::A_OffMsg + pb * kMsgSlot;
+      uint8_t* prow = msg + half * kKChunkBytes;
+      const float nrm = -rmfs;
+      float psum = 0.f;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        float e[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int i = q * 8 + u;
+          e[u] = (full_blk || c0 + i < nv) ? ex2_approx(fmaf(s[i], p.scale_log2, nrm)) : 0.f;
+          psum += e[u];
+        }
+        *(uint4*)(prow + sw128_off((uint32_t)r, (uint32_t)q)) =
+            make_uint4(pack_bf16x2(e[0], e[1]), pack_bf16x2(e[2], e[3]), pack_bf16x2(e[4], e[5]), pack_bf16x2(e[6], e[7]));
+      }
+      se += psum;
+      const bool last = (j == nb - 1);
+      float* tr = (float*)(msg + kMsgPBytes);
+      if (half == 0) tr[r] = alpha;
+      if (last) {  // total normaliser of this piece (both halves)
+        sebuf[half * 128 + r] = se;
+        if (!group_sync(c, nsync)) { ok = false; break; }
+        if (half == 0) {
+          const float se_tot = se + sebuf[128 + r];
+          const bool has = se_tot > 0.f;
+          tr[128 + r] = has ? 1.f / se_tot : 0.f;
+          tr[256 + r] = has ? (rmfs + log2f(se_tot)) * kLn2 : -INFINITY;
+        }
+      }
+      fence_proxy_async_smem();
+      if (!group_sync(c, nsync)) { ok = false; break; }
+      if (sw == 0 && lane == 0)
+        bulk_s2cluster(peer_msg + (uint32_t)pb * kMsgSlot, c.sbase + Y::A_OffMsg + (uint32_t)pb * kMsgSlot, kMsgBytes,
+                       peer_pin_full + 8u * (uint32_t)pb);
+    }
+    ++item;
+  }
+  if (!ok && lane == 0) set_abort(c);
+}
+
+// ============================================================================ PV side
+template <bool kFp8>
+__device__ void pv_gather(const Ctx& c, const FwdParams& p) {
+  using Y = Lay<kFp8>;
+  uint8_t* smem = c.smem;
+  const int warp = c.warp, lane = c.lane;
+  const int gw = (warp == 1) ? 0 : warp - 7;  // 0..8
+  const int gt = gw * 32 + lane;
+  constexpr int kGT = kGatherWarpsB * 32;
+  const int* lists = (const int*)(smem + Y::OffIdx);
+  const uint32_t nblk = blocks_of_pair(p, c.pair);
+  bool ok = true;
+  if constexpr (kFp8) {
+    // Per 16-row group one raw unit: the first 528 bytes of each row (512 e4m3 + 4 fp32 scales),
+    // staged two units ahead, then dequantised into the MN-major V row-group ring.
+    const uint32_t nunits = nblk * (uint32_t)kGroupsPerBlock;
+    auto issue = [&](uint32_t u) -> bool {
+      const uint32_t b = u / (uint32_t)kGroupsPerBlock;
+      const int g = (int)(u % (uint32_t)kGroupsPerBlock), rs = (int)(u % kRawSlots);
+      if (!wait(c, RAW_EMPTY + rs, ((u / kRawSlots) & 1u) ^ 1u)) return false;
+      if (g == 0 && !wait(c, IDX_FULL + (int)(b % kIdxSlots), (b / kIdxSlots) & 1u)) return false;
+      const int* l = lists + (int)(b % kIdxSlots) * kIdxSlotInts + g * kVGroupRows;
+      const uint32_t dst = c.sbase + Y::B_OffRaw + (uint32_t)rs * kRawBSlot;
+      for (int q = gt; q < kVGroupRows * 33; q += kGT) {
+        const int rr = q / 33, pc = q - rr * 33;
+        cp_async16(dst + (uint32_t)q * 16u, p.kv + (size_t)l[rr] * kFp8RowBytes + 16 * pc);
+      }
+      cp_async_arrive(c.bar(RAW_FULL + rs));
+      return true;
+    };
+    auto consume = [&](uint32_t u) -> bool {
+      const uint32_t b = u / (uint32_t)kGroupsPerBlock;
+      const int g = (int)(u % (uint32_t)kGroupsPerBlock), rs = (int)(u % kRawSlots);
+      if (!wait(c, RAW_FULL + rs, (u / kRawSlots) & 1u)) return false;
+      const int s = (int)(u % Y::kVSlots);
+      if (!wait(c, B_V_EMPTY + s, ((u / Y::kVSlots) & 1u) ^ 1u)) return false;
+      const uint8_t* raw = smem + Y::B_OffRaw + rs * kRawBSlot;
+      uint8_t* vd = smem + Y::B_OffV + s * kVGroupBytes;
+      for (int q = gt; q < kVGroupRows * 32; q += kGT) {
+        const int rr = q >> 5, pc = q & 31;
+        const uint8_t* rrow = raw + rr * kRawBRowBytes;
+        uint4 o0, o1;
+        dequant16(*(const uint4*)(rrow + pc * 16), *(const float*)(rrow + 512 + 4 * (pc >> 3)), o0, o1);
+        uint8_t* chunk = vd + (pc >> 2) * 2048;
+        *(uint4*)(chunk + sw128_off((uint32_t)rr, (uint32_t)(2 * (pc & 3)))) = o0;
+        *(uint4*)(chunk + sw128_off((uint32_t)rr, (uint32_t)(2 * (pc & 3) + 1))) = o1;
+      }
+      mbar_arrive(c.bar(B_V_FULL + s));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(c.bar(RAW_EMPTY + rs));
+      if (g == kGroupsPerBlock - 1 && lane == 0) mbar_arrive(c.bar(IDX_EMPTY + (int)(b % kIdxSlots)));
+      return true;
+    };
+    for (uint32_t u = 0; u < 2u && u < nunits && ok; ++u) ok = issue(u);
+    for (uint32_t u = 0; u < nunits && ok; ++u) {
+      if (u + 2u < nunits) ok = issue(u + 2u);
+      if (ok) ok = consume(u);
+    }
+    if (!ok) set_abort(c);
+  } else {
+    uint32_t gseq = 0;
+    for (uint32_t b = 0; b < nblk && ok; ++b) {
+      const int slot = (int)(b % kIdxSlots);
+      if (!wait(c, IDX_FULL + slot, (b / kIdxSlots) & 1u)) { ok = false; break; }
+      const int* l = lists + slot * kIdxSlotInts;
+      for (int g = 0; g < kGroupsPerBlock; ++g, ++gseq) {
+        const int s = (int)(gseq % Y::kVSlots);
+        if (!wait(c, B_V_EMPTY + s, ((gseq / Y::kVSlots) & 1u) ^ 1u)) { ok = false; break; }
+        const uint32_t dst = c.sbase + Y::B_OffV + (uint32_t)s * kVGroupBytes;
+        for (int q = gt; q < 1024; q += kGT) {
+          const int rr = q >> 6, ch = (q >> 3) & 7, p16 = q & 7;
+          cp_async16(dst + (uint32_t)ch * 2048u + sw128_off((uint32_t)rr, (uint32_t)p16),
+                     p.kv + (size_t)l[g * kVGroupRows + rr] * (kDQK * 2) + ch * 128 + p16 * 16);
+        }
+        cp_async_arrive(c.bar(B_V_FULL + s));
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(c.bar(IDX_EMPTY + slot));
+    }
+    if (!ok) set_abort(c);
+    const uint32_t first = gseq > (uint32_t)Y::kVSlots ? gseq - Y::kVSlots : 0u;
+    for (uint32_t q = first; q < gseq; ++q)
+      mbar_wait(c.bar(B_V_FULL + (int)(q % Y::kVSlots)), (q / Y::kVSlots) & 1u, kWaitLimitNs, nullptr);
+  }
+}
+
+template <bool kFp8>
+__device__ void pv_mma(const Ctx& c, const FwdParams& p) {
+  using Y = Lay<kFp8>;
+  if (c.lane == 0) {
+    PieceIter it;
+    it.init(p.cum, p.s_q, c.pair, p.npairs);
+    Piece pc;
+    uint32_t gseq = 0, blk = 0, item = 0;
+    bool ok = true;
+    while (ok && it.next(pc)) {
+      const int nb = pc.lb1 - pc.lb0;
+      for (int j = 0; j < nb && ok; ++j, ++blk) {
+        const int pb = (int)(blk & 1u);
+        if (!wait(c, B_PIN_FULL + pb, (blk >> 1) & 1u) || !wait(c, B_RESC_DONE + pb, (blk >> 1) & 1u)) {
+          ok = false;
+          break;
+        }
+        if (j == 0 && !wait(c, B_O_FREE, (item & 1u) ^ 1u)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t pmsg = c.sbase + Y::B_OffMsg + (uint32_t)pb * kMsgSlot;
+        for (int g = 0; g < kGroupsPerBlock; ++g, ++gseq) {
+          const int s = (int)(gseq % Y::kVSlots);
+          if (!wait(c, B_V_FULL + s, (gseq / Y::kVSlots) & 1u)) { ok = false; break; }
+          fence_proxy_async_smem();
+          tc_fence_after();
+          const uint64_t adesc = smem_desc(pmsg + (uint32_t)(g >> 2) * kKChunkBytes + (uint32_t)(g & 3) * 32u, 16, 1024);
+          const uint32_t vs = c.sbase + Y::B_OffV + (uint32_t)s * kVGroupBytes;
+          const uint32_t acc = (j > 0 || g > 0) ? 1u : 0u;
+          mma_ss(c.tmem + 0, adesc, smem_desc(vs, 2048, 1024), kIdescPV, acc);
+          mma_ss(c.tmem + 256, adesc, smem_desc(vs + 4u * 2048u, 2048, 1024), kIdescPV, acc);
+          mma_commit(c.bar(B_V_EMPTY + s));
+        }
+        if (!ok) break;
+        mma_commit(c.bar(B_PV_DONE + pb));
+        if (j == nb - 1) mma_commit(c.bar(B_O_FULL));
+      }
+      ++item;
+    }
+    if (!ok) set_abort(c);
+    mma_commit(c.bar(B_DRAIN));
+    mbar_wait(c.bar(B_DRAIN), 0, kWaitLimitNs, nullptr);
+  }
+  __syncwarp();
+}
+
+// Message slots: arm the receive barrier for the next message, then hand the slot back to the QK side.
+__device__ __forceinline__ void pv_slot_return(const Ctx& c, const FwdParams& p) {
+  if (c.lane == 0) {
+    const uint32_t peer_pout_empty = mapa_shared(c.bars + 8u * (uint32_t)A_POUT_EMPTY, c.peer);
+    const uint32_t nblk = blocks_of_pair(p, c.pair);
+    bool ok = true;
+    for (uint32_t b = 0; b < nblk && b < 2; ++b) mbar_arrive_expect_tx(c.bar(B_PIN_FULL + (int)b), kMsgBytes);
+    for (uint32_t b = 0; b < nblk; ++b) {
+      const int pb = (int)(b & 1u);
+      if (!wait(c, B_PV_DONE + pb, (b >> 1) & 1u)) { ok = false; break; }
+      if (b + 2 < nblk) mbar_arrive_expect_tx(c.bar(B_PIN_FULL + pb), kMsgBytes);
+      mbar_arrive_remote(peer_pout_empty + 8u * (uint32_t)pb);
+    }
+    if (!ok) set_abort(c);
+  }
+  __syncwarp();
+}
+
+template <bool kFp8>
+__device__ void pv_epilogue(const Ctx& c, const FwdParams& p) {
+  using Y = Lay<kFp8>;
+  uint8_t* smem = c.smem;
+  const int lane = c.lane;
+  const int quarter = c.warp & 3;
+  const int r = quarter * 32 + lane;
+  const uint32_t trow = c.tmem + ((uint32_t)(quarter * 32) << 16);
+  PieceIter it;
+  it.init(p.cum, p.s_q, c.pair, p.npairs);
+  Piece pc;
+  uint32_t blk = 0, item = 0;
+  bool ok = true;
+  while (ok && it.next(pc)) {
+    const int nb = pc.lb1 - pc.lb0;
+    float inv = 0.f, lse_val = -INFINITY;
+    for (int j = 0; j < nb; ++j, ++blk) {
+      const int pb = (int)(blk & 1u);
+      if (!wait(c, B_PIN_FULL + pb, (blk >> 1) & 1u)) { ok = false; break; }
+      const float* tr = (const float*)(smem + Y::B_OffMsg + pb * kMsgSlot + kMsgPBytes);
+      const float alpha = tr[r];
+      if (j == nb - 1) { inv = tr[128 + r]; lse_val = tr[256 + r]; }
+      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+        // O holds earlier blocks of this token: rescale it once the previous P@V is done
+        const uint32_t bp = blk - 1u;
+        if (!wait(c, B_PV_DONE + (int)(bp & 1u), (bp >> 1) & 1u)) { ok = false; break; }
+        tc_fence_after();
+#pragma unroll 1
+        for (int cc = 0; cc < 16; ++cc) {
+          uint32_t v[32];
+          tmem_ld32(trow + (uint32_t)(cc * 32), v);
+          tmem_wait_ld();
+          reg_fence(v);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
+          tmem_st32(trow + (uint32_t)(cc * 32), v);
+        }
+        tmem_wait_st();
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(c.bar(B_RESC_DONE + pb));
+    }
+    if (!ok) break;
+    // ---- epilogue: O / Z -> bf16 (or the normalised fp32 partial of a split token)
+    if (!wait(c, B_O_FULL, item & 1u)) { ok = false; break; }
+    tc_fence_after();
+    const bool live = r < p.h_q;
+#pragma unroll 1
+    for (int cc = 0; cc < 16; ++cc) {
+      uint32_t v[32];
+      const int col = cc * 32;
+      tmem_ld32(trow + (uint32_t)col, v);
+      tmem_wait_ld();
+      reg_fence(v);
+      if (live) {
+        if (pc.full) {
+          uint4* dst = (uint4*)(p.out + ((size_t)pc.t * p.h_q + r) * kDV + col);
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            uint4 w;
+            w.x = pack_bf16x2(__uint_as_float(v[8 * u + 0]) * inv, __uint_as_float(v[8 * u + 1]) * inv);
+            w.y = pack_bf16x2(__uint_as_float(v[8 * u + 2]) * inv, __uint_as_float(v[8 * u + 3]) * inv);
+            w.z = pack_bf16x2(__uint_as_float(v[8 * u + 4]) * inv, __uint_as_float(v[8 * u + 5]) * inv);
+            w.w = pack_bf16x2(__uint_as_float(v[8 * u + 6]) * inv, __uint_as_float(v[8 * u + 7]) * inv);
+            dst[u] = w;
+          }
+        } else {
+          float4* dst = (float4*)(p.part_o + ((size_t)pc.slot * p.h_q + r) * kDV + col);
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            dst[u] = make_float4(__uint_as_float(v[4 * u]) * inv, __uint_as_float(v[4 * u + 1]) * inv,
+                                 __uint_as_float(v[4 * u + 2]) * inv, __uint_as_float(v[4 * u + 3]) * inv);
+        }
+      }
+    }
+    if (live) {
+      if (pc.full) p.lse[(size_t)pc.t * p.h_q + r] = lse_val;
+      else p.part_lse[(size_t)pc.slot * p.h_q + r] = lse_val;
+    }
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(c.bar(B_O_FREE));
+    ++item;
+  }
+  if (!ok && lane == 0) set_abort(c);
+}
+
+}  // namespace fwd
+
+template <bool kFp8>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(fwd::kThreads, 1) dsa_fwd_kernel(const FwdParams p) {
+  using namespace fwd;
+  using Y = Lay<kFp8>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  Ctx c;
+  c.smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  c.sbase = smem_u32(c.smem);
+  c.bars = c.sbase + Y::OffBar;
+  c.warp = threadIdx.x >> 5;
+  c.lane = threadIdx.x & 31;
+  c.rank = cluster_ctarank();
+  c.peer = c.rank ^ 1u;
+  c.pair = (int)(blockIdx.x >> 1);
+  volatile uint32_t* tmem_base_ptr = (volatile uint32_t*)(c.smem + Y::OffMisc);
+  c.abort_flag = (volatile int*)(c.smem + Y::OffMisc + 16);
+  c.peer_abort = mapa_shared(smem_u32((const void*)c.abort_flag), c.peer);
+  c.status = p.ctrl + kCtrlStatus;
+
+  if (threadIdx.x == 0) {
+    const int gwarps = (c.rank == 0) ? kGatherWarpsA : kGatherWarpsB;
+    for (int q = 0; q < kIdxSlots; ++q) {
+      mbar_init(c.bar(IDX_FULL + q), 1);
+      mbar_init(c.bar(IDX_EMPTY + q), gwarps);
+    }
+    for (int q = 0; q < kRawSlots; ++q) {
+      mbar_init(c.bar(RAW_FULL + q), gwarps * 32);
+      mbar_init(c.bar(RAW_EMPTY + q), gwarps);
+    }
+    if (c.rank == 0) {
+      for (int s = 0; s < Y::kKSlots; ++s) {
+        mbar_init(c.bar(A_K_FULL + s), kGatherWarpsA * 32);
+        mbar_init(c.bar(A_K_EMPTY + s), 1);
+      }
+      for (int b = 0; b < 2; ++b) {
+        mbar_init(c.bar(A_S_FULL + b), 1);
+        mbar_init(c.bar(A_S_EMPTY + b), kSoftmaxWarps);
+        mbar_init(c.bar(A_POUT_EMPTY + b), 1);
+      }
+      mbar_init(c.bar(A_Q_FULL), kSoftmaxWarps);
+      mbar_init(c.bar(A_Q_FREE), 1);
+      mbar_init(c.bar(A_SMX_SYNC), kSoftmaxWarps);
+      mbar_init(c.bar(A_DRAIN), 1);
+    } else {
+      for (int s = 0; s < Y::kVSlots; ++s) {
+        mbar_init(c.bar(B_V_FULL + s), kGatherWarpsB * 32);
+        mbar_init(c.bar(B_V_EMPTY + s), 1);
+      }
+      for (int b = 0; b < 2; ++b) {
+        mbar_init(c.bar(B_PIN_FULL + b), 1);
+        mbar_init(c.bar(B_RESC_DONE + b), kEpiWarps);
+        mbar_init(c.bar(B_PV_DONE + b), 1);
+      }
+      mbar_init(c.bar(B_O_FULL), 1);
+      mbar_init(c.bar(B_O_FREE), kEpiWarps);
+      mbar_init(c.bar(B_DRAIN), 1);
+    }
+    *c.abort_flag = 0;
+    fence_mbar_init_cluster();
+  }
+  if (c.warp == 3) {
+    tmem_alloc(smem_u32((const void*)tmem_base_ptr), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  cluster_sync();  // the peer's barriers are initialised before any remote arrive or copy
+  c.tmem = *tmem_base_ptr;
+
+  const int w = c.warp;
+  if (w == 0) {
+    index_compactor<kFp8>(c, p);
+  } else if (w == 2) {
+    if (c.rank == 0) qk_mma<kFp8>(c, p);
+    else pv_mma<kFp8>(c, p);
+  } else if (c.rank == 0) {
+    if (w == 1 || w >= 12) qk_gather<kFp8>(c, p);
+    else if (w >= 4) qk_softmax<kFp8>(c, p);
+  } else {
+    if (w == 1 || w >= 8) pv_gather<kFp8>(c, p);
+    else if (w == 3) pv_slot_return(c, p);
+    else if (w >= 4) pv_epilogue<kFp8>(c, p);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (c.warp == 3) tmem_dealloc(c.tmem, kTmemCols);
+  cluster_sync();  // no remote copy or arrive may target an exited CTA
+}
+
+// Largest number of 2-CTA clusters of the kernel that fit at once on the current device.
+template <bool kFp8>
+int max_active_pairs_impl() {
+  static int cached = -1;
+  static int cached_dev = -1;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cached >= 0 && cached_dev == dev) return cached;
+  constexpr int smem = fwd::Lay<kFp8>::SmemAlloc;
+  if (cudaFuncSetAttribute(dsa_fwd_kernel<kFp8>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+    return 0;
+  int sms = 0;
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * sms, 1, 1);
+  cfg.blockDim = dim3(fwd::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  int nclusters = 0;
+  if (cudaOccupancyMaxActiveClusters(&nclusters, dsa_fwd_kernel<kFp8>, &cfg) != cudaSuccess || nclusters <= 0) {
+    cudaGetLastError();
+    return 0;
+  }
+  cached = nclusters;
+  cached_dev = dev;
+  return cached;
+}
+
+template <bool kFp8>
+cudaError_t launch_impl(const FwdParams& p, cudaStream_t stream) {
+  constexpr int smem = fwd::Lay<kFp8>::SmemAlloc;
+  cudaError_t e = cudaFuncSetAttribute(dsa_fwd_kernel<kFp8>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  dsa_fwd_kernel<kFp8><<<2 * p.npairs, fwd::kThreads, smem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace dsa

@@ -2,7 +2,7 @@
 
 Small cases compare every output element; the full-size workloads compare a
 sample of tokens that the oracle computes one by one.  Cases span several
-index blocks of 64, ragged tails (topk % 64 != 0), -1 and out-of-range slots,
+index blocks of 128, ragged tails (topk % 128 != 0), -1 and out-of-range slots,
 fully masked tokens, duplicates, h_q < 128, and enough tokens that the work
 sequence is cut across CTA pairs (exercising the merge of split tokens).
 """
@@ -106,6 +106,32 @@ def test_rescale_fires_with_wide_logits():
     _check(W.small_random(14, 3, 128, 4000, 1024, q_sigma=4.0))
 
 
+# ---------------------------------------------------------------- FP8-e4m3 KV cache (656-byte rows)
+
+@pytest.mark.parametrize("s_q,h_q,s_kv,topk,bad", [
+    (3, 128, 700, 128, 0.0),     # exactly one block
+    (3, 128, 900, 129, 0.0),     # one block + a 1-row tail
+    (5, 128, 3000, 300, 0.1),    # ragged tail and -1 slots
+    (4, 64, 5000, 2048, 0.05),   # many blocks, h_q = 64
+    (6, 16, 300, 127, 0.3),      # h_q = 16, heavy masking
+])
+def test_fp8_small_shapes(s_q, h_q, s_kv, topk, bad):
+    _check(W.small_random(s_q * 1000 + topk + 7, s_q, h_q, s_kv, topk, kv_format="fp8", invalid_frac=bad, q_sigma=2.0))
+
+
+def test_fp8_masked_tokens_and_split_work():
+    wl = W.small_random(17, 200, 128, 6000, 512, kv_format="fp8", invalid_frac=0.05, q_sigma=2.0)
+    idx = wl.indices.clone()
+    idx[3, :] = -1
+    idx[5, 100:] = -1
+    wl.indices = idx
+    _check(wl, tokens=list(range(0, 200, 9)) + [3, 5])
+
+
+def test_fp8_tiny_decode_shape():
+    _check(W.decode_fp8(n_seq=4, s_kv_per_seq=4096, topk=2048))
+
+
 # ---------------------------------------------------------------- full-size workloads (sampled tokens)
 
 @pytest.mark.slow
@@ -131,3 +157,10 @@ def test_long_prefill_full_size_sampled():
     rng = np.random.default_rng(1)
     tokens = sorted(set(rng.choice(wl.s_q, 24, replace=False).tolist()) | {0, wl.s_q - 1})
     _check(wl, tokens=tokens, out=out, lse=lse)
+
+
+@pytest.mark.slow
+def test_decode_fp8_full_size_sampled():
+    wl = W.decode_fp8()
+    out, lse = P.run_gpu(wl)
+    _check(wl, tokens=[0, 1, 50, 99, 127], out=out, lse=lse)
