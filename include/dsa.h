@@ -107,6 +107,27 @@ DSA_API dsa_status dsa_sparse_attn_fwd_fp8kv(const void* q, const void* kv_fp8, 
                                      int s_kv, int topk, float sm_scale, void* out, float* lse, void* workspace,
                                      size_t workspace_bytes, cudaStream_t stream);
 
+/* Allocation-free variant of dsa_sparse_attn_fwd, for callers that cannot
+ * allocate device memory themselves (code that runs where cudaMalloc is not
+ * available or not allowed, such as inside a custom allocator, or a plugin
+ * that is handed only its input and output buffers).  The pages have no
+ * counterpart; this is a convenience of this library.  Arguments as for
+ * dsa_sparse_attn_fwd, without the workspace: the call uses one scratch
+ * array compiled into the library instead (about 40 MiB per device, held by
+ * every GPU that loads the library until the process exits).
+ * Limits: s_q <= 8192, h_q <= 128, and at most 80 resident SM pairs on the
+ * device; larger calls return DSA_ERR_WORKSPACE and launch nothing.
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture.  Every call shares the one array and leaves its
+ * contents behind (the call clears what must start at zero itself), so calls
+ * whose work overlaps on the GPU (concurrent streams, several host threads)
+ * race: serialise them.  Device-side timeouts are recorded in the array, not
+ * readable through dsa_read_device_status.  No allocation of any kind is made. */
+DSA_API dsa_status dsa_sparse_attn_fwd_noalloc(const void* q, const void* kv, const int32_t* indices, int s_q, int h_q,
+                                               int s_kv, int topk, float sm_scale, void* out, float* lse,
+                                               cudaStream_t stream);
+
 /* Synchronises `stream` and returns the device-side status a previous forward
  * call left in `workspace` (DSA_OK or DSA_ERR_DEVICE_TIMEOUT), or DSA_ERR_CUDA
  * if the synchronisation itself failed. */

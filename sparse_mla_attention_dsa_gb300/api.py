@@ -112,3 +112,20 @@ def dsa_set_timing_events(before=None, after=None) -> None:
         _lib.load().dsa_set_timing_events(ctypes.c_void_p(0), ctypes.c_void_p(0))
         return
     _lib.load().dsa_set_timing_events(ctypes.c_void_p(before.cuda_event), ctypes.c_void_p(after.cuda_event))
+
+
+def dsa_sparse_attn_fwd_noalloc(q, kv, indices, sm_scale, out, lse, stream=None):
+    """The bf16 forward without a workspace, for callers that cannot allocate device memory.
+
+    The library uses its own built-in scratch array instead (limits: s_q <= 8192,
+    h_q <= 128).  `out` and `lse` must be given (nothing is allocated here).
+    Calls that overlap on the GPU share that array and race; serialise them.
+    """
+    _check(q, kv, indices, KV_BF16)
+    s_q, h_q, _ = q.shape
+    st = _lib.load().dsa_sparse_attn_fwd_noalloc(_ptr(q), _ptr(kv), _ptr(indices), s_q, h_q, kv.shape[0],
+                                                 indices.shape[1], ctypes.c_float(sm_scale), _ptr(out), _ptr(lse),
+                                                 _stream_handle(stream))
+    if st != 0:
+        raise _lib.DsaError(st, "dsa_sparse_attn_fwd_noalloc")
+    return out, lse

@@ -20,10 +20,10 @@ struct WorkspaceLayout {
   size_t ctrl, nvalid, cum, part_lse, part_o, total;
 };
 
-inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+constexpr size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-inline WorkspaceLayout workspace_layout(int s_q, int h_q, int npairs) {
-  WorkspaceLayout L;
+constexpr WorkspaceLayout workspace_layout(int s_q, int h_q, int npairs) {
+  WorkspaceLayout L{};
   size_t off = 0;
   L.ctrl = off;     off += 256;
   L.nvalid = off;   off += align_up(sizeof(int) * (size_t)(s_q > 0 ? s_q : 1), 256);
