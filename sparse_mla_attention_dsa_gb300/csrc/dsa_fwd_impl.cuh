@@ -54,8 +54,13 @@ namespace fwd {
 constexpr int kThreads = 512;
 constexpr int kSoftmaxWarps = 8;                 // QK side, warps 4..11
 constexpr int kEpiWarps = 4;                     // PV side, warps 4..7
-constexpr int kGatherWarpsA = 5;                 // QK side: warps 1, 12..15
-constexpr int kGatherWarpsB = 9;                 // PV side: warps 1, 8..15
+constexpr int kGatherWarpsA = 5;                 // FP8, QK side: warps 1, 12..15
+constexpr int kGatherWarpsB = 9;                 // FP8, PV side: warps 1, 8..15
+// bf16 rows: bulk-copy issuers and in-place transposers
+constexpr int kIssuersA = 4;                     // QK side: warps 12..15
+constexpr int kTransA = 2;                       // QK side: warps 1, 3
+constexpr int kIssuersB = 6;                     // PV side: warps 8..13
+constexpr int kTransB = 3;                       // PV side: warps 1, 14, 15
 constexpr int kIdxSlots = 4;                     // ring of per-block index lists
 constexpr int kIdxSlotInts = kBT + 4;            // 128 row ids + count
 
@@ -72,6 +77,22 @@ constexpr int kVGroupBytes = kVGroupRows * 1024; // 16 rows x 512 columns bf16 =
 constexpr int kGroupsPerBlock = 128 / kVGroupRows;
 constexpr int kIdxRing = 256;
 constexpr int kMaxKSlots = 8, kMaxVSlots = 9;
+// bf16 QK side: the K operand of a block as two halves of 64 rows (N = 64 MMAs), each half 8 groups of
+// 8 rows; a group's latent part is 8 SW128 atoms (one per 64-column chunk, 8 KB), its rope part one atom
+constexpr int kUnitBytes = 8 * 1024;             // 8 rows x 512 latent columns after the in-place transpose
+constexpr int kHalfLatBytes = 8 * kUnitBytes;    // 64 KB
+constexpr int kHalfRopeBytes = 8 * 1024;         // 8 KB
+constexpr int kGroupsPerHalf = 8;
+// Share of rows fetched by bulk copies (then transposed) versus cp.async straight into the swizzled
+// layout.  A GB300 SM's copy engine takes one 1 KB bulk copy per ~37 cycles and cp.async runs beside it,
+// but inside this pipeline cp.async rows land later than bulk rows and lengthen the fill of a buffer, so
+// measured on GB300 all-bulk is fastest (prefill 4.19 ms vs 4.46 ms with 3/8 of the rows by cp.async).
+constexpr int kBulkGroupsA = 8;                  // QK side: groups [0, kBulkGroupsA) of each half by bulk copy
+constexpr int kBulkUnit1B = 8;                   // PV side: unit 1 of slot groups [0, kBulkUnit1B) by bulk copy
+
+// cp.async of 8 rows' latent 1024 bytes straight into 8 SW128 atoms (one warp, 16 pieces per lane; a warp
+// instruction covers 4 rows x 128 bytes of one atom).
+__device__ __forceinline__ void cp_async_unit(uint32_t dst, const uint8_t* kv, const int* rows, int lane);
 // FP8 rows: raw units staged before dequantisation
 constexpr int kRawSlots = 4;
 constexpr int kRawASlot = 128 * 64;              // QK side unit: 128 rows x 64 bytes (64 e4m3 or 32 bf16)
@@ -84,15 +105,16 @@ __host__ __device__ constexpr int align1k(int x) { return (x + 1023) / 1024 * 10
 // Shared-memory layout of each side for one KV format.
 template <bool kFp8>
 struct Lay {
-  static constexpr int kKSlots = kFp8 ? 6 : 8;
+  static constexpr int kKSlots = kFp8 ? 6 : 0;   // FP8: ring of 128-row x 64-column chunks
   static constexpr int kVSlots = kFp8 ? 7 : 9;
-  // QK side (cluster rank 0)
+  // QK side (cluster rank 0).  bf16: latent halves [2][8 groups][8 atoms], then rope atoms [2][8 groups].
   static constexpr int A_OffK = 0;
-  static constexpr int A_OffRaw = A_OffK + kKSlots * kKChunkBytes;
+  static constexpr int A_OffKR = A_OffK + (kFp8 ? 0 : 2 * kHalfLatBytes);
+  static constexpr int A_OffRaw = kFp8 ? A_OffK + kKSlots * kKChunkBytes : A_OffKR + 2 * kHalfRopeBytes;
   static constexpr int A_OffScales = A_OffRaw + (kFp8 ? kRawSlots * kRawASlot : 0);
   static constexpr int A_OffQRope = A_OffScales + (kFp8 ? 2 * kScaleSlot : 0);
-  static constexpr int A_OffMsg = align1k(A_OffQRope + kKChunkBytes);
-  static constexpr int A_OffMax = A_OffMsg + 2 * kMsgSlot;  // [2 halves][128] float
+  static constexpr int A_OffMsg = align1k(A_OffQRope + kKChunkBytes);  // one outgoing message buffer
+  static constexpr int A_OffMax = A_OffMsg + kMsgSlot;  // [2 halves][128] float
   static constexpr int A_OffSe = A_OffMax + 2 * 128 * 4;
   static constexpr int A_End = A_OffSe + 2 * 128 * 4;
   // PV side (cluster rank 1)
@@ -120,18 +142,22 @@ enum BarCommon {
 enum BarA {
   A_K_FULL = BAR_COMMON_END, A_K_EMPTY = A_K_FULL + kMaxKSlots, A_S_FULL = A_K_EMPTY + kMaxKSlots,
   A_S_EMPTY = A_S_FULL + 2, A_Q_FULL = A_S_EMPTY + 2, A_Q_FREE, A_POUT_EMPTY, A_SMX_SYNC = A_POUT_EMPTY + 2, A_DRAIN,
-  A_NUM
+  A_KH_FULL, A_KH_EMPTY = A_KH_FULL + 2, A_MSG_FREE = A_KH_EMPTY + 2, A_NUM,
+  A_LAND = A_K_FULL  // bf16: landing barriers of the 16 groups of a block (spans the FP8 K_FULL/K_EMPTY slots)
 };
 enum BarB {
   B_V_FULL = BAR_COMMON_END, B_V_EMPTY = B_V_FULL + kMaxVSlots, B_PIN_FULL = B_V_EMPTY + kMaxVSlots,
-  B_RESC_DONE = B_PIN_FULL + 2, B_PV_DONE = B_RESC_DONE + 2, B_O_FULL = B_PV_DONE + 2, B_O_FREE, B_DRAIN, B_NUM
+  B_RESC_DONE = B_PIN_FULL + 2, B_PV_DONE = B_RESC_DONE + 2, B_O_FULL = B_PV_DONE + 2, B_O_FREE, B_DRAIN,
+  B_V_LAND, B_NUM = B_V_LAND + kMaxVSlots
 };
+static_assert((int)A_LAND + 16 <= (int)A_S_FULL, "bf16 landing barriers fit in the K slots");
 static_assert((int)A_NUM <= 56 && (int)B_NUM <= 56, "barrier slots");
 
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmQ = 0;     // QK side: Q latent [0, 256) (bf16 pairs), S tiles [256, 384) and [384, 512)
 constexpr uint32_t kTmS = 256;
 constexpr uint32_t kIdescQK = idesc_bf16_f32(128, kBT, 0, 0);
+constexpr uint32_t kIdescQK64 = idesc_bf16_f32(128, 64, 0, 0);
 constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 256, 0, 1);
 
 constexpr float kThresLog2 = 6.0f * 1.4426950408889634f;  // RESCALE_THRES = 6 (natural log) in log2 units
@@ -182,8 +208,42 @@ __device__ __forceinline__ uint32_t sw128_off(uint32_t row, uint32_t chunk16) {
   return (row >> 3) * 1024 + (row & 7) * 128 + ((chunk16 ^ (row & 7)) << 4);
 }
 
+// In-place re-layout of one 8-row unit: 8 rows of 512 bf16 landed as plain rows (row r at r*1024) become
+// 8 SW128 atoms (64-column chunk c at c*1024, row r at r*128 inside it, 16-byte pieces XOR-swizzled by r).
+// As 128-byte segments this is an 8x8 transpose; the segments with (r + c) even and with (r + c) odd are
+// each closed under it, so a warp moves each class through registers (8 pieces per lane) in one step.
+__device__ __forceinline__ void transpose_unit(uint8_t* un, int lane) {
+#pragma unroll
+  for (int ph = 0; ph < 2; ++ph) {
+    uint4 v[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const int sidx = q * 4 + (lane >> 3), k = lane & 7;
+      const int r = sidx >> 2, c = 2 * (sidx & 3) + ((r + ph) & 1);
+      v[q] = *(const uint4*)(un + r * 1024 + c * 128 + k * 16);
+    }
+    __syncwarp();
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const int sidx = q * 4 + (lane >> 3), k = lane & 7;
+      const int r = sidx >> 2, c = 2 * (sidx & 3) + ((r + ph) & 1);
+      *(uint4*)(un + c * 1024 + sw128_off((uint32_t)r, (uint32_t)k)) = v[q];
+    }
+    __syncwarp();
+  }
+}
+
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_unit(uint32_t dst, const uint8_t* kv, const int* rows, int lane) {
+#pragma unroll 4
+  for (int j = 0; j < 16; ++j) {
+    const int q = j * 32 + lane;
+    const int ch = q >> 6, r = (q >> 3) & 7, k = q & 7;
+    cp_async16(dst + (uint32_t)(ch * 1024) + sw128_off((uint32_t)r, (uint32_t)k),
+               kv + (size_t)rows[r] * (kDQK * 2) + ch * 128 + k * 16);
+  }
 }
 __device__ __forceinline__ void cp_async_arrive(uint32_t bar) {
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
@@ -328,9 +388,9 @@ __device__ void index_compactor(const Ctx& c, const FwdParams& p) {
 }
 
 // ============================================================================ QK side
-template <bool kFp8>
-__device__ void qk_gather(const Ctx& c, const FwdParams& p) {
-  using Y = Lay<kFp8>;
+// FP8 rows: cp.async into a raw ring, dequantised by the same warps into the K chunk ring.
+static __device__ void qk_gather_fp8(const Ctx& c, const FwdParams& p) {
+  using Y = Lay<true>;
   uint8_t* smem = c.smem;
   const int warp = c.warp, lane = c.lane;
   const int gw = (warp == 1) ? 0 : warp - 11;  // 0..4
@@ -339,7 +399,7 @@ __device__ void qk_gather(const Ctx& c, const FwdParams& p) {
   const int* lists = (const int*)(smem + Y::OffIdx);
   const uint32_t nblk = blocks_of_pair(p, c.pair);
   bool ok = true;
-  if constexpr (kFp8) {
+  {
     // Per block 10 raw units of 128 rows x 64 bytes: latent chunks 0..7 (e4m3) and rope halves 8..9
     // (bf16); the block's scales ride with unit 0.  Units are staged in a 4-slot ring two units ahead,
     // then dequantised (latent) or copied (rope) into the swizzled K chunk ring.
@@ -395,31 +455,75 @@ __device__ void qk_gather(const Ctx& c, const FwdParams& p) {
       if (ok) ok = consume(u);
     }
     if (!ok) set_abort(c);
-  } else {
-    uint32_t cseq = 0;
-    for (uint32_t b = 0; b < nblk && ok; ++b) {
-      const int slot = (int)(b % kIdxSlots);
-      if (!wait(c, IDX_FULL + slot, (b / kIdxSlots) & 1u)) { ok = false; break; }
-      const int* l = lists + slot * kIdxSlotInts;
-      for (int k = 0; k < kChunksPerBlock; ++k, ++cseq) {
-        const int s = (int)(cseq % Y::kKSlots);
-        if (!wait(c, A_K_EMPTY + s, ((cseq / Y::kKSlots) & 1u) ^ 1u)) { ok = false; break; }
-        const uint32_t dst = c.sbase + Y::A_OffK + (uint32_t)s * kKChunkBytes;
-        for (int q = gt; q < 1024; q += kGT) {
-          const int r = q >> 3, p16 = q & 7;
-          cp_async16(dst + sw128_off((uint32_t)r, (uint32_t)p16), p.kv + (size_t)l[r] * (kDQK * 2) + k * 128 + p16 * 16);
-        }
-        cp_async_arrive(c.bar(A_K_FULL + s));
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(c.bar(IDX_EMPTY + slot));
-    }
-    if (!ok) set_abort(c);
-    // every issued copy lands before the CTA may exit
-    const uint32_t first = cseq > (uint32_t)Y::kKSlots ? cseq - Y::kKSlots : 0u;
-    for (uint32_t q = first; q < cseq; ++q)
-      mbar_wait(c.bar(A_K_FULL + (int)(q % Y::kKSlots)), (q / Y::kKSlots) & 1u, kWaitLimitNs, nullptr);
   }
+}
+
+// bf16 rows, issuers (warps 12..15): group g of block b (rows 8g..8g+7) goes to half g / 8.  Lane r < 8
+// bulk-copies the 1024 latent bytes of row r as they are (the transposer lays them out afterwards); all
+// lanes cp.async the 128 rope bytes of the 8 rows straight into the group's swizzled rope atom.  The
+// group's landing barrier completes on the bulk bytes plus one cp.async arrival per lane.
+static __device__ void qk_issue_bf16(const Ctx& c, const FwdParams& p) {
+  using Y = Lay<false>;
+  const int lane = c.lane, i = c.warp - 12;
+  const int* lists = (const int*)(c.smem + Y::OffIdx);
+  const uint32_t nblk = blocks_of_pair(p, c.pair);
+  uint32_t issued = 0;
+  bool ok = true;
+  for (uint32_t b = 0; b < nblk && ok; ++b) {
+    const int slot = (int)(b % kIdxSlots);
+    if (!wait(c, IDX_FULL + slot, (b / kIdxSlots) & 1u)) { ok = false; break; }
+    const int* l = lists + slot * kIdxSlotInts;
+    for (int g = i; g < 2 * kGroupsPerHalf; g += kIssuersA) {
+      const int h = g / kGroupsPerHalf, gg = g % kGroupsPerHalf;
+      if (!wait(c, A_KH_EMPTY + h, (b & 1u) ^ 1u)) { ok = false; break; }
+      const uint32_t land = c.bar(A_LAND + g);
+      const bool bulk = gg < kBulkGroupsA;
+      const uint32_t unit = c.sbase + Y::A_OffK + (uint32_t)(h * kHalfLatBytes + gg * kUnitBytes);
+      if (lane == 0) mbar_arrive_expect_tx(land, bulk ? (uint32_t)kUnitBytes : 0u);
+      __syncwarp();
+      if (bulk) {
+        if (lane < 8) bulk_g2s(unit + (uint32_t)(lane * 1024), p.kv + (size_t)l[g * 8 + lane] * (kDQK * 2), 1024u, land);
+      } else {
+        cp_async_unit(unit, p.kv, l + g * 8, lane);
+      }
+      const uint32_t rope = c.sbase + Y::A_OffKR + (uint32_t)(h * kHalfRopeBytes + gg * 1024);
+#pragma unroll
+      for (int q = lane; q < 64; q += 32) {
+        const int r = q >> 3, k = q & 7;
+        cp_async16(rope + sw128_off((uint32_t)r, (uint32_t)k), p.kv + (size_t)l[g * 8 + r] * (kDQK * 2) + 1024 + k * 16);
+      }
+      cp_async_arrive(land);
+    }
+    if (!ok) break;
+    issued = b + 1;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(c.bar(IDX_EMPTY + slot));
+  }
+  if (!ok) set_abort(c);
+  // the copies of the last block issued land before the CTA may exit
+  if (issued > 0)
+    for (int g = i; g < 2 * kGroupsPerHalf; g += kIssuersA)
+      mbar_wait(c.bar(A_LAND + g), (issued - 1) & 1u, kWaitLimitNs, nullptr);
+}
+
+// bf16 rows, transposers (warps 1 and 3): once a group has landed, turn its latent rows into SW128
+// atoms in place and count the group towards its half.
+static __device__ void qk_transpose_bf16(const Ctx& c, const FwdParams& p) {
+  using Y = Lay<false>;
+  const int lane = c.lane, t = (c.warp == 1) ? 0 : 1;
+  const uint32_t nblk = blocks_of_pair(p, c.pair);
+  bool ok = true;
+  for (uint32_t b = 0; b < nblk && ok; ++b) {
+    for (int g = t; g < 2 * kGroupsPerHalf; g += kTransA) {
+      const int h = g / kGroupsPerHalf, gg = g % kGroupsPerHalf;
+      if (!wait(c, A_LAND + g, b & 1u)) { ok = false; break; }
+      if (gg < kBulkGroupsA) transpose_unit(c.smem + Y::A_OffK + h * kHalfLatBytes + gg * kUnitBytes, lane);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(c.bar(A_KH_FULL + h));
+    }
+  }
+  if (!ok) set_abort(c);
 }
 
 template <bool kFp8>
@@ -440,20 +544,46 @@ __device__ void qk_mma(const Ctx& c, const FwdParams& p) {
         if (!wait(c, A_S_EMPTY + sb, ((blk >> 1) & 1u) ^ 1u)) { ok = false; break; }
         tc_fence_after();
         const uint32_t dS = c.tmem + kTmS + (uint32_t)sb * kBT;
-        for (int k = 0; k < kChunksPerBlock; ++k, ++cseq) {
-          const int s = (int)(cseq % Y::kKSlots);
-          if (!wait(c, A_K_FULL + s, (cseq / Y::kKSlots) & 1u)) { ok = false; break; }
-          fence_proxy_async_smem();  // generic-proxy writes (cp.async / dequant) -> tensor core reads
-          tc_fence_after();
-          const uint32_t chunk = c.sbase + Y::A_OffK + (uint32_t)s * kKChunkBytes;
+        if constexpr (!kFp8) {
+          // bf16: each half of 64 rows as soon as its 8 groups are laid out (N = 64), then free it
+          for (int h = 0; h < 2 && ok; ++h) {
+            if (!wait(c, A_KH_FULL + h, blk & 1u)) { ok = false; break; }
+            fence_proxy_async_smem();  // generic-proxy writes (transposer / cp.async) -> tensor core reads
+            tc_fence_after();
+            // descriptors built once; a step of 16 columns (32 bytes) or one atom (1 KB) only moves the
+            // start-address field (bits 0..13, address / 16, no carry below 256 KB)
+            const uint64_t lat = smem_desc(c.sbase + Y::A_OffK + (uint32_t)(h * kHalfLatBytes), 16, kUnitBytes);
+            const uint64_t rope = smem_desc(c.sbase + Y::A_OffKR + (uint32_t)(h * kHalfRopeBytes), 16, 1024);
+            const uint64_t qr = smem_desc(qrope, 16, 1024);
+            const uint32_t dh = dS + (uint32_t)(h * 64), qa = c.tmem + kTmQ;
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t bdesc = smem_desc(chunk + (uint32_t)kk * 32u, 16, 1024);
-            const uint32_t acc = (k > 0 || kk > 0) ? 1u : 0u;
-            if (k < 8) mma_ts(dS, c.tmem + kTmQ + (uint32_t)(k * 32 + kk * 8), bdesc, kIdescQK, acc);
-            else mma_ss(dS, smem_desc(qrope + (uint32_t)kk * 32u, 16, 1024), bdesc, kIdescQK, acc);
+            for (int k = 0; k < 8; ++k)
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk)
+                mma_ts(dh, qa + (uint32_t)(k * 32 + kk * 8), lat + (uint64_t)(k * 64 + kk * 2), kIdescQK64,
+                       (k > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              mma_ss(dh, qr + (uint64_t)(kk * 2), rope + (uint64_t)(kk * 2), kIdescQK64, 1u);
+            mma_commit(c.bar(A_KH_EMPTY + h));
           }
-          mma_commit(c.bar(A_K_EMPTY + s));
+        } else {
+          // FP8: the ring of 128-row chunks, one chunk of 64 columns at a time (N = 128)
+          for (int k = 0; k < kChunksPerBlock; ++k, ++cseq) {
+            const int s = (int)(cseq % Y::kKSlots);
+            if (!wait(c, A_K_FULL + s, (cseq / Y::kKSlots) & 1u)) { ok = false; break; }
+            fence_proxy_async_smem();  // generic-proxy writes (cp.async / dequant) -> tensor core reads
+            tc_fence_after();
+            const uint32_t chunk = c.sbase + Y::A_OffK + (uint32_t)s * kKChunkBytes;
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint64_t bdesc = smem_desc(chunk + (uint32_t)kk * 32u, 16, 1024);
+              const uint32_t acc = (k > 0 || kk > 0) ? 1u : 0u;
+              if (k < 8) mma_ts(dS, c.tmem + kTmQ + (uint32_t)(k * 32 + kk * 8), bdesc, kIdescQK, acc);
+              else mma_ss(dS, smem_desc(qrope + (uint32_t)kk * 32u, 16, 1024), bdesc, kIdescQK, acc);
+            }
+            mma_commit(c.bar(A_K_EMPTY + s));
+          }
         }
         if (!ok) break;
         mma_commit(c.bar(A_S_FULL + sb));
@@ -524,6 +654,8 @@ __device__ void qk_softmax(const Ctx& c, const FwdParams& p) {
     for (int j = 0; j < nb; ++j, ++blk) {
       const int sb = (int)(blk & 1u);
       float s[64];
+      // the one outgoing buffer is free once the previous message has landed in the peer
+      if (blk > 0 && !wait(c, A_MSG_FREE, (blk - 1u) & 1u, true)) { ok = false; break; }
       if (!wait(c, A_S_FULL + sb, (blk >> 1) & 1u)) { ok = false; break; }
       tc_fence_after();
       {
@@ -569,7 +701,7 @@ __device__ void qk_softmax(const Ctx& c, const FwdParams& p) {
       // ---- message slot free?  then exponentials straight into the P tile (this half = one SW128 chunk)
       const int pb = (int)(blk & 1u);
       if (!wait(c, A_POUT_EMPTY + pb, ((blk >> 1) & 1u) ^ 1u, true)) { ok = false; break; }
-      uint8_t* msg = smem + Y::A_OffMsg + pb * kMsgSlot;
+      uint8_t* msg = smem + Y::A_OffMsg;
       uint8_t* prow = msg + half * kKChunkBytes;
       const float nrm = -rmfs;
       float psum = 0.f;
@@ -602,7 +734,7 @@ __device__ void qk_softmax(const Ctx& c, const FwdParams& p) {
       fence_proxy_async_smem();
       if (!group_sync(c, nsync)) { ok = false; break; }
       if (sw == 0 && lane == 0)
-        bulk_s2cluster(peer_msg + (uint32_t)pb * kMsgSlot, c.sbase + Y::A_OffMsg + (uint32_t)pb * kMsgSlot, kMsgBytes,
+        bulk_s2cluster(peer_msg + (uint32_t)pb * kMsgSlot, c.sbase + Y::A_OffMsg, kMsgBytes,
                        peer_pin_full + 8u * (uint32_t)pb);
     }
     ++item;
@@ -611,9 +743,9 @@ __device__ void qk_softmax(const Ctx& c, const FwdParams& p) {
 }
 
 // ============================================================================ PV side
-template <bool kFp8>
-__device__ void pv_gather(const Ctx& c, const FwdParams& p) {
-  using Y = Lay<kFp8>;
+// FP8 rows: cp.async into a raw ring, dequantised by the same warps into the V row-group ring.
+static __device__ void pv_gather_fp8(const Ctx& c, const FwdParams& p) {
+  using Y = Lay<true>;
   uint8_t* smem = c.smem;
   const int warp = c.warp, lane = c.lane;
   const int gw = (warp == 1) ? 0 : warp - 7;  // 0..8
@@ -622,7 +754,7 @@ __device__ void pv_gather(const Ctx& c, const FwdParams& p) {
   const int* lists = (const int*)(smem + Y::OffIdx);
   const uint32_t nblk = blocks_of_pair(p, c.pair);
   bool ok = true;
-  if constexpr (kFp8) {
+  {
     // Per 16-row group one raw unit: the first 528 bytes of each row (512 e4m3 + 4 fp32 scales),
     // staged two units ahead, then dequantised into the MN-major V row-group ring.
     const uint32_t nunits = nblk * (uint32_t)kGroupsPerBlock;
@@ -669,31 +801,66 @@ __device__ void pv_gather(const Ctx& c, const FwdParams& p) {
       if (ok) ok = consume(u);
     }
     if (!ok) set_abort(c);
-  } else {
-    uint32_t gseq = 0;
-    for (uint32_t b = 0; b < nblk && ok; ++b) {
-      const int slot = (int)(b % kIdxSlots);
-      if (!wait(c, IDX_FULL + slot, (b / kIdxSlots) & 1u)) { ok = false; break; }
-      const int* l = lists + slot * kIdxSlotInts;
-      for (int g = 0; g < kGroupsPerBlock; ++g, ++gseq) {
-        const int s = (int)(gseq % Y::kVSlots);
-        if (!wait(c, B_V_EMPTY + s, ((gseq / Y::kVSlots) & 1u) ^ 1u)) { ok = false; break; }
-        const uint32_t dst = c.sbase + Y::B_OffV + (uint32_t)s * kVGroupBytes;
-        for (int q = gt; q < 1024; q += kGT) {
-          const int rr = q >> 6, ch = (q >> 3) & 7, p16 = q & 7;
-          cp_async16(dst + (uint32_t)ch * 2048u + sw128_off((uint32_t)rr, (uint32_t)p16),
-                     p.kv + (size_t)l[g * kVGroupRows + rr] * (kDQK * 2) + ch * 128 + p16 * 16);
-        }
-        cp_async_arrive(c.bar(B_V_FULL + s));
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(c.bar(IDX_EMPTY + slot));
-    }
-    if (!ok) set_abort(c);
-    const uint32_t first = gseq > (uint32_t)Y::kVSlots ? gseq - Y::kVSlots : 0u;
-    for (uint32_t q = first; q < gseq; ++q)
-      mbar_wait(c.bar(B_V_FULL + (int)(q % Y::kVSlots)), (q / Y::kVSlots) & 1u, kWaitLimitNs, nullptr);
   }
+}
+
+// bf16 rows, issuers (warps 8..13): slot group g of block b holds rows 16g..16g+15 as two 8-row units;
+// lane j < 16 bulk-copies the 1024 latent bytes (= V) of row 16g + j into unit j / 8 as a plain row.
+static __device__ void pv_issue_bf16(const Ctx& c, const FwdParams& p) {
+  using Y = Lay<false>;
+  const int lane = c.lane, i = c.warp - 8;
+  const int* lists = (const int*)(c.smem + Y::OffIdx);
+  const uint32_t nblk = blocks_of_pair(p, c.pair);
+  uint32_t done = 0;  // groups of all blocks before the current one
+  bool ok = true;
+  for (uint32_t b = 0; b < nblk && ok; ++b) {
+    const int slot = (int)(b % kIdxSlots);
+    if (!wait(c, IDX_FULL + slot, (b / kIdxSlots) & 1u)) { ok = false; break; }
+    const int* l = lists + slot * kIdxSlotInts;
+    for (int g = i; g < kGroupsPerBlock; g += kIssuersB) {
+      const uint32_t gs = done + (uint32_t)g;
+      const int s = (int)(gs % Y::kVSlots);
+      if (!wait(c, B_V_EMPTY + s, ((gs / Y::kVSlots) & 1u) ^ 1u)) { ok = false; break; }
+      const uint32_t land = c.bar(B_V_LAND + s);
+      const bool bulk1 = g < kBulkUnit1B;
+      const uint32_t grp = c.sbase + Y::B_OffV + (uint32_t)(s * kVGroupBytes);
+      if (lane == 0) mbar_arrive_expect_tx(land, bulk1 ? (uint32_t)kVGroupBytes : (uint32_t)kUnitBytes);
+      __syncwarp();
+      if (lane < (bulk1 ? kVGroupRows : 8))
+        bulk_g2s(grp + (uint32_t)((lane >> 3) * kUnitBytes + (lane & 7) * 1024),
+                 p.kv + (size_t)l[g * kVGroupRows + lane] * (kDQK * 2), 1024u, land);
+      if (!bulk1) cp_async_unit(grp + (uint32_t)kUnitBytes, p.kv, l + g * kVGroupRows + 8, lane);
+      cp_async_arrive(land);  // one arrival per lane, whether or not it issued cp.async
+    }
+    if (!ok) break;
+    done += (uint32_t)kGroupsPerBlock;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(c.bar(IDX_EMPTY + slot));
+  }
+  if (!ok) set_abort(c);
+  // the copies of the last ring round land before the CTA may exit
+  for (uint32_t gs = done > (uint32_t)Y::kVSlots ? done - Y::kVSlots : 0u; gs < done; ++gs)
+    if ((int)(gs % (uint32_t)kGroupsPerBlock) % kIssuersB == i)
+      mbar_wait(c.bar(B_V_LAND + (int)(gs % Y::kVSlots)), (gs / Y::kVSlots) & 1u, kWaitLimitNs, nullptr);
+}
+
+// bf16 rows, transposers (warps 1, 14, 15): lay out both units of a landed slot group and hand it to the MMA.
+static __device__ void pv_transpose_bf16(const Ctx& c, const FwdParams& p) {
+  using Y = Lay<false>;
+  const int lane = c.lane, t = (c.warp == 1) ? 0 : c.warp - 13;
+  const uint32_t total = blocks_of_pair(p, c.pair) * (uint32_t)kGroupsPerBlock;
+  bool ok = true;
+  for (uint32_t gs = (uint32_t)t; gs < total; gs += kTransB) {
+    const int s = (int)(gs % Y::kVSlots);
+    if (!wait(c, B_V_LAND + s, (gs / Y::kVSlots) & 1u)) { ok = false; break; }
+    uint8_t* grp = c.smem + Y::B_OffV + s * kVGroupBytes;
+    transpose_unit(grp, lane);
+    if ((int)(gs % (uint32_t)kGroupsPerBlock) < kBulkUnit1B) transpose_unit(grp + kUnitBytes, lane);
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(c.bar(B_V_FULL + s));
+  }
+  if (!ok) set_abort(c);
 }
 
 template <bool kFp8>
@@ -724,8 +891,12 @@ __device__ void pv_mma(const Ctx& c, const FwdParams& p) {
           const uint64_t adesc = smem_desc(pmsg + (uint32_t)(g >> 2) * kKChunkBytes + (uint32_t)(g & 3) * 32u, 16, 1024);
           const uint32_t vs = c.sbase + Y::B_OffV + (uint32_t)s * kVGroupBytes;
           const uint32_t acc = (j > 0 || g > 0) ? 1u : 0u;
-          mma_ss(c.tmem + 0, adesc, smem_desc(vs, 2048, 1024), kIdescPV, acc);
-          mma_ss(c.tmem + 256, adesc, smem_desc(vs + 4u * 2048u, 2048, 1024), kIdescPV, acc);
+          // V of 16 rows, MN-major: 64-column chunks LBO apart, the two 8-row atoms along K SBO apart.
+          // bf16 groups are two transposed units (chunk stride 1 KB, unit stride 8 KB); FP8 groups are
+          // dequantised chunk-major (chunk stride 2 KB, atom stride 1 KB).
+          constexpr uint32_t kLbo = kFp8 ? 2048u : 1024u, kSbo = kFp8 ? 1024u : (uint32_t)kUnitBytes;
+          mma_ss(c.tmem + 0, adesc, smem_desc(vs, kLbo, kSbo), kIdescPV, acc);
+          mma_ss(c.tmem + 256, adesc, smem_desc(vs + 4u * kLbo, kLbo, kSbo), kIdescPV, acc);
           mma_commit(c.bar(B_V_EMPTY + s));
         }
         if (!ok) break;
@@ -745,11 +916,14 @@ __device__ void pv_mma(const Ctx& c, const FwdParams& p) {
 __device__ __forceinline__ void pv_slot_return(const Ctx& c, const FwdParams& p) {
   if (c.lane == 0) {
     const uint32_t peer_pout_empty = mapa_shared(c.bars + 8u * (uint32_t)A_POUT_EMPTY, c.peer);
+    const uint32_t peer_msg_free = mapa_shared(c.bars + 8u * (uint32_t)A_MSG_FREE, c.peer);
     const uint32_t nblk = blocks_of_pair(p, c.pair);
     bool ok = true;
     for (uint32_t b = 0; b < nblk && b < 2; ++b) mbar_arrive_expect_tx(c.bar(B_PIN_FULL + (int)b), kMsgBytes);
     for (uint32_t b = 0; b < nblk; ++b) {
       const int pb = (int)(b & 1u);
+      if (!wait(c, B_PIN_FULL + pb, (b >> 1) & 1u)) { ok = false; break; }
+      mbar_arrive_remote(peer_msg_free);  // the QK side may refill its outgoing buffer
       if (!wait(c, B_PV_DONE + pb, (b >> 1) & 1u)) { ok = false; break; }
       if (b + 2 < nblk) mbar_arrive_expect_tx(c.bar(B_PIN_FULL + pb), kMsgBytes);
       mbar_arrive_remote(peer_pout_empty + 8u * (uint32_t)pb);
@@ -870,19 +1044,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(fwd::kThreads, 1) ds
 
   if (threadIdx.x == 0) {
     const int gwarps = (c.rank == 0) ? kGatherWarpsA : kGatherWarpsB;
+    const int list_users = kFp8 ? gwarps : (c.rank == 0 ? kIssuersA : kIssuersB);
     for (int q = 0; q < kIdxSlots; ++q) {
       mbar_init(c.bar(IDX_FULL + q), 1);
-      mbar_init(c.bar(IDX_EMPTY + q), gwarps);
+      mbar_init(c.bar(IDX_EMPTY + q), list_users);
     }
     for (int q = 0; q < kRawSlots; ++q) {
       mbar_init(c.bar(RAW_FULL + q), gwarps * 32);
       mbar_init(c.bar(RAW_EMPTY + q), gwarps);
     }
     if (c.rank == 0) {
-      for (int s = 0; s < Y::kKSlots; ++s) {
-        mbar_init(c.bar(A_K_FULL + s), kGatherWarpsA * 32);
-        mbar_init(c.bar(A_K_EMPTY + s), 1);
+      if constexpr (kFp8) {
+        for (int s = 0; s < Y::kKSlots; ++s) {
+          mbar_init(c.bar(A_K_FULL + s), kGatherWarpsA * 32);
+          mbar_init(c.bar(A_K_EMPTY + s), 1);
+        }
+      } else {
+        for (int g = 0; g < 2 * kGroupsPerHalf; ++g) mbar_init(c.bar(A_LAND + g), 1 + 32);  // expect_tx + cp.async
+        for (int h = 0; h < 2; ++h) {
+          mbar_init(c.bar(A_KH_FULL + h), kGroupsPerHalf);
+          mbar_init(c.bar(A_KH_EMPTY + h), 1);
+        }
       }
+      mbar_init(c.bar(A_MSG_FREE), 1);
       for (int b = 0; b < 2; ++b) {
         mbar_init(c.bar(A_S_FULL + b), 1);
         mbar_init(c.bar(A_S_EMPTY + b), kSoftmaxWarps);
@@ -894,8 +1078,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(fwd::kThreads, 1) ds
       mbar_init(c.bar(A_DRAIN), 1);
     } else {
       for (int s = 0; s < Y::kVSlots; ++s) {
-        mbar_init(c.bar(B_V_FULL + s), kGatherWarpsB * 32);
+        mbar_init(c.bar(B_V_FULL + s), kFp8 ? kGatherWarpsB * 32 : 1);
         mbar_init(c.bar(B_V_EMPTY + s), 1);
+        mbar_init(c.bar(B_V_LAND + s), 1 + 32);  // expect_tx + cp.async
       }
       for (int b = 0; b < 2; ++b) {
         mbar_init(c.bar(B_PIN_FULL + b), 1);
@@ -926,12 +1111,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(fwd::kThreads, 1) ds
     if (c.rank == 0) qk_mma<kFp8>(c, p);
     else pv_mma<kFp8>(c, p);
   } else if (c.rank == 0) {
-    if (w == 1 || w >= 12) qk_gather<kFp8>(c, p);
-    else if (w >= 4) qk_softmax<kFp8>(c, p);
+    if constexpr (kFp8) {
+      if (w == 1 || w >= 12) qk_gather_fp8(c, p);
+      else if (w >= 4) qk_softmax<kFp8>(c, p);
+    } else {
+      if (w >= 12) qk_issue_bf16(c, p);
+      else if (w >= 4) qk_softmax<kFp8>(c, p);
+      else qk_transpose_bf16(c, p);  // warps 1, 3
+    }
   } else {
-    if (w == 1 || w >= 8) pv_gather<kFp8>(c, p);
-    else if (w == 3) pv_slot_return(c, p);
-    else if (w >= 4) pv_epilogue<kFp8>(c, p);
+    if constexpr (kFp8) {
+      if (w == 1 || w >= 8) pv_gather_fp8(c, p);
+      else if (w == 3) pv_slot_return(c, p);
+      else if (w >= 4) pv_epilogue<kFp8>(c, p);
+    } else {
+      if (w >= 8 && w < 14) pv_issue_bf16(c, p);
+      else if (w == 1 || w >= 14) pv_transpose_bf16(c, p);
+      else if (w == 3) pv_slot_return(c, p);
+      else if (w >= 4) pv_epilogue<kFp8>(c, p);
+    }
   }
 
   tc_fence_before();
