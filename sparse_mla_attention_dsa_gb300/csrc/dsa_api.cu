@@ -86,64 +86,106 @@ __global__ void __launch_bounds__(kPrepWarps * 32) dsa_prep_kernel(const int32_t
 //   lse = ln sum_j exp(lse_j),   out = sum_j exp(lse_j - lse) * out_j.
 // This step is not on the pages; it makes the blockwise result of several
 // pair ranges equal to the result of one range (same exact value).
-// CTA p handles the token containing boundary b_p = p*T/P when b_p is the first
-// boundary strictly inside it.
+// CTA (p, y) handles heads [8y, 8y + 8) of the token containing boundary
+// b_p = p*T/P when b_p is the first boundary strictly inside it; one warp per
+// head, 16 output columns per lane.
 // ----------------------------------------------------------------------------
 __device__ __forceinline__ long long boundary(int p, long long T, int P) { return (long long)p * T / P; }
 
-__global__ void __launch_bounds__(256) dsa_combine_kernel(const int* __restrict__ cum, const int* __restrict__ ctrl,
-                                                          int s_q, int h_q, int npairs,
-                                                          const float* __restrict__ part_lse,
-                                                          const float* __restrict__ part_o, uint16_t* out, float* lse) {
-  const int p = blockIdx.x;
-  if (p == 0) return;
-  const long long T = ctrl[kCtrlTotalBlocks];
-  const long long bp = boundary(p, T, npairs);
-  if (bp >= T) return;
-  int lo = 0, hi = s_q - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (cum[mid] <= bp) lo = mid; else hi = mid - 1;
+constexpr int kCombineWarps = 8;
+
+// Largest t in [0, s_q) with cum[t] <= key (cum ascending, cum[0] = 0 <= key): 32-way search by one warp.
+__device__ int find_token(const int* cum, int s_q, long long key, int lane) {
+  int lo = 0, hi = s_q - 1;  // answer in [lo, hi]
+  while (hi > lo) {
+    const int span = hi - lo;
+    const int step = (span + 31) / 32;
+    const int pos = lo + lane * step;
+    const bool le = pos <= hi && (long long)__ldg(cum + pos) <= key;
+    const unsigned m = __ballot_sync(0xffffffffu, le);
+    const int last = 31 - __clz(m);                  // lane 0 always qualifies (pos = lo)
+    lo = lo + last * step;
+    hi = min(hi, lo + step - 1);
   }
-  const int t = lo;
-  const long long c0 = cum[t], c1 = cum[t + 1];
-  if (bp == c0) return;                              // boundary at a token start: nothing split here
-  if (boundary(p - 1, T, npairs) > c0) return;       // an earlier boundary inside t handles it
-  // pairs covering blocks c0 .. c1-1: pair(g) = ((g + 1) * P - 1) / T
-  const int pfirst = (int)(((c0 + 1) * npairs - 1) / T);
-  const int plast = (int)((c1 * npairs - 1) / T);
-  constexpr int kMaxPieces = 64;
-  __shared__ int slots[kMaxPieces];
-  __shared__ int nslots;
-  if (threadIdx.x == 0) {
-    int ns = 0;
-    for (int q = pfirst; q <= plast && ns < kMaxPieces; ++q) {
-      const long long bq = boundary(q, T, npairs), bq1 = boundary(q + 1, T, npairs);
-      if (bq1 <= bq) continue;                       // empty range
-      slots[ns++] = (bq >= c0) ? 2 * q : 2 * q + 1;  // t is q's first token iff q starts inside t
+  return lo;
+}
+
+__global__ void __launch_bounds__(kCombineWarps * 32) dsa_combine_kernel(const int* __restrict__ cum,
+                                                                         const int* __restrict__ ctrl, int s_q, int h_q,
+                                                                         int npairs, const float* __restrict__ part_lse,
+                                                                         const float* __restrict__ part_o, uint16_t* out,
+                                                                         float* lse) {
+  __shared__ int tok_s;
+  __shared__ long long c0_s, c1_s;
+  const int p = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long T = ctrl[kCtrlTotalBlocks];
+  if (warp == 0) {
+    int tok = -1;
+    long long c0 = 0, c1 = 0;
+    const long long bp = boundary(p, T, npairs);
+    if (p > 0 && bp < T) {
+      const int t = find_token(cum, s_q, bp, lane);
+      c0 = cum[t];
+      c1 = cum[t + 1];
+      // split at bp, and bp is the first boundary inside t
+      if (bp != c0 && boundary(p - 1, T, npairs) <= c0) tok = t;
     }
-    nslots = ns;
+    if (lane == 0) { tok_s = tok; c0_s = c0; c1_s = c1; }
   }
   __syncthreads();
-  const int ns = nslots;
-  for (int h = 0; h < h_q; ++h) {
-    float m = -INFINITY;
-    for (int j = 0; j < ns; ++j) m = fmaxf(m, part_lse[(size_t)slots[j] * h_q + h]);
-    float wsum = 0.f;
-    float w[kMaxPieces];
-    for (int j = 0; j < ns; ++j) {
-      const float l = part_lse[(size_t)slots[j] * h_q + h];
-      w[j] = (m == -INFINITY) ? 0.f : expf(l - m);
-      wsum += w[j];
-    }
-    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-    for (int d = threadIdx.x; d < kDV; d += blockDim.x) {
-      float acc = 0.f;
-      for (int j = 0; j < ns; ++j) acc += w[j] * part_o[((size_t)slots[j] * h_q + h) * kDV + d];
-      out[((size_t)t * h_q + h) * kDV + d] = __bfloat16_as_ushort(__float2bfloat16_rn(acc * inv));
-    }
-    if (threadIdx.x == 0) lse[(size_t)t * h_q + h] = (wsum > 0.f) ? m + logf(wsum) : -INFINITY;
+  const int t = tok_s;
+  const int h = blockIdx.y * kCombineWarps + warp;
+  if (t < 0 || h >= h_q) return;
+  const long long c0 = c0_s, c1 = c1_s;
+  // pairs covering blocks c0 .. c1-1: pair(g) = ((g + 1) * P - 1) / T; a pair whose range starts inside t
+  // holds t as its first piece (slot 2q), otherwise as its second (slot 2q + 1)
+  const int pfirst = (int)(((c0 + 1) * npairs - 1) / T);
+  const int plast = (int)((c1 * npairs - 1) / T);
+  auto slot_lse = [&](int q, int& slot) -> float {
+    const long long bq = boundary(q, T, npairs), bq1 = boundary(q + 1, T, npairs);
+    if (bq1 <= bq) { slot = -1; return -INFINITY; }  // empty range
+    slot = (bq >= c0) ? 2 * q : 2 * q + 1;
+    return __ldg(part_lse + (size_t)slot * h_q + h);
+  };
+  float m = -INFINITY;
+  for (int q = pfirst + lane; q <= plast; q += 32) {
+    int sl;
+    m = fmaxf(m, slot_lse(q, sl));
   }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  float wsum = 0.f;
+  float4 acc[4];
+#pragma unroll
+  for (int u = 0; u < 4; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+  const int d0 = lane * 16;
+  for (int q = pfirst; q <= plast; ++q) {
+    int sl;
+    const float l = slot_lse(q, sl);
+    if (sl < 0 || m == -INFINITY) continue;
+    const float w = expf(l - m);
+    wsum += w;
+    const float4* src = reinterpret_cast<const float4*>(part_o + ((size_t)sl * h_q + h) * kDV + d0);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const float4 v = __ldg(src + u);
+      acc[u].x += w * v.x; acc[u].y += w * v.y; acc[u].z += w * v.z; acc[u].w += w * v.w;
+    }
+  }
+  const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+  uint32_t pk[8];
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    pk[2 * u] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(acc[u].x * inv)) |
+                ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(acc[u].y * inv)) << 16);
+    pk[2 * u + 1] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(acc[u].z * inv)) |
+                    ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(acc[u].w * inv)) << 16);
+  }
+  uint4* dst = reinterpret_cast<uint4*>(out + ((size_t)t * h_q + h) * kDV + d0);
+  dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+  dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+  if (lane == 0) lse[(size_t)t * h_q + h] = (wsum > 0.f) ? m + logf(wsum) : -INFINITY;
 }
 
 // Output for s_kv == 0: no row can be valid.
@@ -222,8 +264,9 @@ static dsa_status forward(int kv_format, const void* q, const void* kv, const in
   e = (kv_format == DSA_KV_BF16) ? launch_fwd_bf16(p, stream) : launch_fwd_fp8(p, stream);
   if (timed) cudaEventRecord(g_ev_after, stream);
   if (e != cudaSuccess) return DSA_ERR_CUDA;
-  dsa_combine_kernel<<<npairs, 256, 0, stream>>>(p.cum, p.ctrl, s_q, h_q, npairs, p.part_lse, p.part_o,
-                                                 (uint16_t*)out, lse);
+  const dim3 cgrid((unsigned)npairs, (unsigned)((h_q + kCombineWarps - 1) / kCombineWarps));
+  dsa_combine_kernel<<<cgrid, kCombineWarps * 32, 0, stream>>>(p.cum, p.ctrl, s_q, h_q, npairs, p.part_lse, p.part_o,
+                                                               (uint16_t*)out, lse);
   return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
 

@@ -341,13 +341,10 @@ struct IndexRing {
   }
 };
 
+// Index blocks of pair `pair`: its share [pair*T/P, (pair+1)*T/P) of the block sequence.
 __device__ __forceinline__ uint32_t blocks_of_pair(const FwdParams& p, int pair) {
-  PieceIter it;
-  it.init(p.cum, p.s_q, pair, p.npairs);
-  Piece pc;
-  uint32_t n = 0;
-  while (it.next(pc)) n += (uint32_t)(pc.lb1 - pc.lb0);
-  return n;
+  const long long T = p.cum[p.s_q];
+  return (uint32_t)((long long)(pair + 1) * T / p.npairs - (long long)pair * T / p.npairs);
 }
 
 // ============================================================================ both sides: index lists

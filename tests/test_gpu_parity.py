@@ -78,8 +78,13 @@ def test_scheduler_splits_tokens_across_pairs():
 
 
 def test_one_token_spread_over_every_pair():
-    # 32 blocks < number of CTA pairs: one token cut into many pieces, some pairs idle
+    # 16 blocks < number of CTA pairs: one token cut into many pieces, some pairs idle
     _check(W.small_random(12, 1, 128, 8192, 2048, q_sigma=2.0))
+
+
+def test_one_token_cut_into_more_pieces_than_a_warp_has_lanes():
+    # 100 blocks over every CTA pair: the merge sees one piece per pair (more than 32 and more than 64)
+    _check(W.small_random(14, 1, 128, 16384, 12800, q_sigma=2.0))
 
 
 def test_repeatable_and_no_stray_writes():
