@@ -64,7 +64,7 @@ def _peaks():
 
 
 class ClockSampler:
-    """nvidia-smi samples every 200 ms while the timed region runs."""
+    """nvidia-smi samples every 20 ms while the timed region runs."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -75,7 +75,7 @@ class ClockSampler:
         self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
         try:
             self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                                          "-lms", "200", "-i", str(gpu_index)], stdout=self.f,
+                                          "-lms", "20", "-i", str(gpu_index)], stdout=self.f,
                                          stderr=subprocess.DEVNULL)
         except (FileNotFoundError, OSError):
             self.proc = None
@@ -100,6 +100,32 @@ class ClockSampler:
         reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].strip() == "Active"})
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
                 "reasons": reasons, "samples": len(rows)}
+
+
+KERNEL_SOURCES = ("dsa_fwd_impl.cuh", "ptx.cuh", "dsa_internal.h", "dsa_fwd.cu", "dsa_fwd_fp8.cu")
+
+
+def _kernel_sources_sha256() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "sparse_mla_attention_dsa_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def _measured_traffic(workload: str):
+    """DRAM bytes per launch of the attention kernel from the ncu capture recorded in profiles/, or None when
+    there is none for this workload or the kernel sources changed since it was taken."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f)
+    if rec.get("kernel_sources_sha256") != _kernel_sources_sha256():
+        return None
+    w = rec.get("workloads", {}).get(workload)
+    return None if w is None else float(w["dram_read_bytes"] + w["dram_write_bytes"])
 
 
 def cpu_oracle_sample(wl, seconds: float, start_token: int = 0):
@@ -277,7 +303,10 @@ def _report(args, wl, flops, ms, kms, e2e_ms, clocks, world):
     else:
         roof = {"bound": "tensor", "achieved": tf_achieved, "peak": peak_tf, "unit": "TFLOP/s",
                 "frac": tf_achieved / peak_tf}
-    roof.update({"traffic": args.traffic, "alg_bytes": abytes, "alg_flops": flops, "peak_source": peak_src,
+    traffic = args.traffic if args.traffic is not None else _measured_traffic(args.workload)
+    if args.s_q is not None and args.workload == "prefill_causal" and args.s_q != 4096 and args.traffic is None:
+        traffic = None  # the recorded capture is of the full-size workload
+    roof.update({"traffic": traffic, "alg_bytes": abytes, "alg_flops": flops, "peak_source": peak_src,
                  "kernel": "dsa_fwd_kernel<%s>" % ("false" if wl.kv_format == "bf16" else "true"),
                  "kernel_ms": kms, "tensor_frac": tf_achieved / peak_tf, "hbm_frac": gbs_achieved / hbm_gbs,
                  "roofline_ms": 1e3 * max(t_flops, t_bytes)})
