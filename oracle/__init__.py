@@ -13,6 +13,8 @@ Modules:
               emulated step by step in float32 with the bf16 cast of S.
   formats     bit-level decoders of bf16 and FP8-e4m3 and of the 656-byte FP8
               KV row.
+  paged       logical positions of a sequence -> rows of a paged KV pool
+              through a block table (the forward itself is unchanged).
 
 Every function is pinned by ``tests/test_oracle*.py`` against values fixed by
 the pages or by mathematics (closed forms, invariants, brute force, library
