@@ -134,6 +134,10 @@ def cpu_oracle_sample(wl, seconds: float, start_token: int = 0):
     qb = wl.q.contiguous().view(torch.int16).numpy().view(np.uint16)
     kvr = wl.kv.contiguous().view(torch.int16).numpy().view(np.uint16) if wl.kv_format == "bf16" else wl.kv.numpy()
     idx = wl.indices.numpy()
+    if wl.meta.get("paged"):  # the oracle's own translation of logical positions to pool rows
+        from oracle import paged as PG
+        idx = PG.logical_to_rows(idx, wl.meta["seq_of_token"].numpy(), wl.meta["block_table"].numpy(),
+                                 wl.meta["page_size"], wl.kv.shape[0])
     flops, n, t0 = 0.0, 0, time.perf_counter()
     t = start_token
     while True:
@@ -203,6 +207,13 @@ def run_gb300(args, rank: int, world: int, local_rank: int):
                      dtype=torch.uint8, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
+
+    if wl.meta.get("paged"):  # logical positions through a block table over a page pool
+        seq, table = wl.meta["seq_of_token"].to(dev), wl.meta["block_table"].to(dev)
+
+        def fwd(q, kv, idx, sm_scale, out, lse, workspace):
+            api.dsa_sparse_attn_fwd_paged(q, kv, idx, seq, table, wl.meta["page_size"], sm_scale, out=out, lse=lse,
+                                          workspace=workspace)
 
     def step():
         fwd(q, kv, idx, wl.sm_scale, out=out, lse=lse, workspace=ws)
@@ -345,7 +356,7 @@ def main():
     ap.add_argument("--s-q", type=int, default=4096, help="query tokens (4096 = the benchmark workload)")
     ap.add_argument("--skip-e2e", action="store_true")
     ap.add_argument("--workload", default="prefill_causal",
-                    choices=["prefill_causal", "decode_bf16", "decode_fp8", "long_prefill", "tiny"])
+                    choices=["prefill_causal", "decode_bf16", "decode_fp8", "long_prefill", "decode_paged", "tiny"])
     ap.add_argument("--traffic", type=float, default=None,
                     help="DRAM bytes per attention-kernel launch from an ncu capture (null when not given)")
     args = ap.parse_args()

@@ -128,6 +128,29 @@ DSA_API dsa_status dsa_sparse_attn_fwd_noalloc(const void* q, const void* kv, co
                                                int s_kv, int topk, float sm_scale, void* out, float* lse,
                                                cudaStream_t stream);
 
+/* The forward over a paged KV cache ("Flash Attention Infer算子性能优化", section
+ * "优化Paged Attention路径": a sequence's KV lives in fixed-size pages of a shared
+ * pool and is reached through a block table).
+ *   kv_format     DSA_KV_BF16 (kv_pool bf16 [n_rows, 576]) or DSA_KV_FP8 (uint8 [n_rows, 656]);
+ *                 the pool holds n_rows / page_size pages of page_size rows, page k at rows
+ *                 [k * page_size, (k + 1) * page_size).
+ *   indices       int32 [s_q, topk]: logical positions in the token's own sequence.
+ *   seq_of_token  int32 [s_q]: the sequence of each query token, in [0, n_seq).
+ *   block_table   int32 [n_seq, max_pages]: physical page of each logical page; < 0 = unmapped.
+ * Position v of a token of sequence s reads pool row
+ *   block_table[s][v / page_size] * page_size + v % page_size;
+ * it is excluded exactly (like -1 in the flat layout) when v < 0, v / page_size >= max_pages,
+ * the table entry is negative, s is outside [0, n_seq) or the row is outside [0, n_rows).
+ * Everything else (q, out, lse, sm_scale, workspace size and use, stream, errors) is as for
+ * dsa_sparse_attn_fwd / dsa_sparse_attn_fwd_fp8kv with s_kv = n_rows; seq_of_token and
+ * block_table need 4-byte alignment, page_size, max_pages, n_seq >= 1 and
+ * n_seq * max_pages < 2^31 (else DSA_ERR_INVALID_ARG). */
+DSA_API dsa_status dsa_sparse_attn_fwd_paged(int kv_format, const void* q, const void* kv_pool, const int32_t* indices,
+                                             const int32_t* seq_of_token, const int32_t* block_table, int s_q,
+                                             int h_q, int n_rows, int topk, int n_seq, int max_pages, int page_size,
+                                             float sm_scale, void* out, float* lse, void* workspace,
+                                             size_t workspace_bytes, cudaStream_t stream);
+
 /* Synchronises `stream` and returns the device-side status a previous forward
  * call left in `workspace` (DSA_OK or DSA_ERR_DEVICE_TIMEOUT), or DSA_ERR_CUDA
  * if the synchronisation itself failed. */

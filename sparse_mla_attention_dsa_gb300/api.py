@@ -86,6 +86,39 @@ def dsa_sparse_attn_fwd_fp8kv(q, kv_fp8, indices, sm_scale, out=None, lse=None, 
                     check_status)
 
 
+def dsa_sparse_attn_fwd_paged(q, kv_pool, indices, seq_of_token, block_table, page_size, sm_scale, kv_format=KV_BF16,
+                              out=None, lse=None, workspace=None, stream=None, check_status=False):
+    """Sparse MLA forward over a paged KV cache: indices [s_q, topk] are logical positions in each token's
+    sequence (seq_of_token int32 [s_q]); block_table int32 [n_seq, max_pages] gives the physical page of each
+    logical page of the pool kv_pool (page k = rows [k * page_size, (k + 1) * page_size))."""
+    _check(q, kv_pool, indices, kv_format)
+    for name, t in (("seq_of_token", seq_of_token), ("block_table", block_table)):
+        if not t.is_cuda or t.dtype != torch.int32 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous int32 CUDA tensor")
+    if seq_of_token.dim() != 1 or seq_of_token.shape[0] != q.shape[0] or block_table.dim() != 2:
+        raise ValueError("seq_of_token must be [s_q] and block_table [n_seq, max_pages]")
+    lib = _lib.load()
+    s_q, h_q, _ = q.shape
+    topk = indices.shape[1]
+    n_seq, max_pages = block_table.shape
+    if out is None:
+        out = torch.empty((s_q, h_q, D_V), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((s_q, h_q), dtype=torch.float32, device=q.device)
+    ws_bytes = int(lib.dsa_sparse_attn_fwd_workspace_size(s_q, h_q, topk, kv_format))
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=q.device)
+    st = lib.dsa_sparse_attn_fwd_paged(kv_format, _ptr(q), _ptr(kv_pool), _ptr(indices), _ptr(seq_of_token),
+                                       _ptr(block_table), s_q, h_q, kv_pool.shape[0], topk, n_seq, max_pages,
+                                       page_size, ctypes.c_float(sm_scale), _ptr(out), _ptr(lse), _ptr(workspace),
+                                       ctypes.c_size_t(workspace.numel()), _stream_handle(stream))
+    if st != 0:
+        raise _lib.DsaError(st, "dsa_sparse_attn_fwd_paged")
+    if check_status:
+        dsa_read_device_status(workspace, stream)
+    return out, lse
+
+
 def dsa_read_device_status(workspace, stream=None) -> int:
     """Synchronise the stream and raise if a kernel reported a device-side timeout."""
     st = int(_lib.load().dsa_read_device_status(_ptr(workspace), _stream_handle(stream)))

@@ -27,20 +27,20 @@ cudaError_t launch_fwd_fp8(const FwdParams& p, cudaStream_t stream);
 // ----------------------------------------------------------------------------
 constexpr int kPrepWarps = 8;
 
-__global__ void __launch_bounds__(kPrepWarps * 32) dsa_prep_kernel(const int32_t* __restrict__ indices, int s_q,
-                                                                   int topk, int s_kv, int* nvalid, int* cum,
-                                                                   int* ctrl) {
+__global__ void __launch_bounds__(kPrepWarps * 32) dsa_prep_kernel(const FwdParams p) {
   __shared__ int is_last;
   __shared__ int part[kPrepWarps * 32];
+  const int s_q = p.s_q, topk = p.topk;
+  int* nvalid = p.nvalid;
+  int* cum = p.cum;
+  int* ctrl = p.ctrl;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * kPrepWarps + warp;
   if (t < s_q) {
-    const int32_t* row = indices + (size_t)t * topk;
+    const int32_t* row = p.indices + (size_t)t * topk;
+    const int seq = token_seq(p, t);
     int c = 0;
-    for (int i = lane; i < topk; i += 32) {
-      const int v = __ldg(row + i);
-      c += (v >= 0 && v < s_kv) ? 1 : 0;
-    }
+    for (int i = lane; i < topk; i += 32) c += resolve_row(p, seq, __ldg(row + i)) >= 0 ? 1 : 0;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
     if (lane == 0) nvalid[t] = c;
@@ -215,7 +215,7 @@ static cudaEvent_t g_ev_before = nullptr, g_ev_after = nullptr;
 
 static dsa_status forward(int kv_format, const void* q, const void* kv, const int32_t* indices, int s_q, int h_q,
                           int s_kv, int topk, float sm_scale, void* out, float* lse, void* workspace,
-                          size_t workspace_bytes, cudaStream_t stream) {
+                          size_t workspace_bytes, cudaStream_t stream, const PagedView* pg = nullptr) {
   if (s_q < 0 || h_q < 1 || h_q > kMaxHeads || s_kv < 0 || topk < 1 || !std::isfinite(sm_scale))
     return DSA_ERR_INVALID_ARG;
   if (s_q == 0) return DSA_OK;
@@ -246,6 +246,7 @@ static dsa_status forward(int kv_format, const void* q, const void* kv, const in
   p.s_kv = s_kv;
   p.topk = topk;
   p.scale_log2 = sm_scale * 1.4426950408889634f;
+  p.pg = pg ? *pg : PagedView{nullptr, nullptr, 1, 1, 1};
   p.ctrl = (int*)(ws + L.ctrl);
   p.nvalid = (int*)(ws + L.nvalid);
   p.cum = (int*)(ws + L.cum);
@@ -255,7 +256,7 @@ static dsa_status forward(int kv_format, const void* q, const void* kv, const in
 
   if (cudaMemsetAsync(p.ctrl, 0, 256, stream) != cudaSuccess) return DSA_ERR_CUDA;
   const int prep_blocks = (s_q + kPrepWarps - 1) / kPrepWarps;
-  dsa_prep_kernel<<<prep_blocks, kPrepWarps * 32, 0, stream>>>(indices, s_q, topk, s_kv, p.nvalid, p.cum, p.ctrl);
+  dsa_prep_kernel<<<prep_blocks, kPrepWarps * 32, 0, stream>>>(p);
   if (cudaGetLastError() != cudaSuccess) return DSA_ERR_CUDA;
 
   cudaError_t e;
@@ -294,6 +295,22 @@ dsa_status dsa_sparse_attn_fwd_fp8kv(const void* q, const void* kv_fp8, const in
                                      size_t workspace_bytes, cudaStream_t stream) {
   return dsa::forward(DSA_KV_FP8, q, kv_fp8, indices, s_q, h_q, s_kv, topk, sm_scale, out, lse, workspace,
                       workspace_bytes, stream);
+}
+
+dsa_status dsa_sparse_attn_fwd_paged(int kv_format, const void* q, const void* kv_pool, const int32_t* indices,
+                                     const int32_t* seq_of_token, const int32_t* block_table, int s_q, int h_q,
+                                     int n_rows, int topk, int n_seq, int max_pages, int page_size, float sm_scale,
+                                     void* out, float* lse, void* workspace, size_t workspace_bytes,
+                                     cudaStream_t stream) {
+  if (kv_format != DSA_KV_BF16 && kv_format != DSA_KV_FP8) return DSA_ERR_INVALID_ARG;
+  if (n_seq < 1 || max_pages < 1 || page_size < 1 || (long long)n_seq * max_pages > 0x7fffffffLL)
+    return DSA_ERR_INVALID_ARG;
+  if (s_q > 0 && (!seq_of_token || !block_table)) return DSA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(seq_of_token) & 3u) || (reinterpret_cast<uintptr_t>(block_table) & 3u))
+    return DSA_ERR_MISALIGNED;
+  const dsa::PagedView pg{block_table, seq_of_token, page_size, max_pages, n_seq};
+  return dsa::forward(kv_format, q, kv_pool, indices, s_q, h_q, n_rows, topk, sm_scale, out, lse, workspace,
+                      workspace_bytes, stream, &pg);
 }
 
 dsa_status dsa_read_device_status(const void* workspace, cudaStream_t stream) {

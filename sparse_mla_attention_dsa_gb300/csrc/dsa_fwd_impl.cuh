@@ -309,9 +309,11 @@ __device__ __forceinline__ bool group_sync(const Ctx& c, uint32_t& n) {
 struct IndexRing {
   int* ring;
   const int32_t* idx_t;
-  int topk, s_kv, head, tail, rp;
-  __device__ void reset(int* r, const int32_t* p, int tk, int skv) {
-    ring = r; idx_t = p; topk = tk; s_kv = skv; head = tail = rp = 0;
+  const FwdParams* prm;
+  int topk, seq, head, tail, rp;
+  __device__ void reset(int* r, const FwdParams& p, int t) {
+    ring = r; prm = &p; idx_t = p.indices + (size_t)t * p.topk; topk = p.topk; seq = token_seq(p, t);
+    head = tail = rp = 0;
   }
   // ensure >= kBT entries (or the token's end) are buffered; returns the count for this block
   __device__ int fill(int lane) {
@@ -323,8 +325,10 @@ struct IndexRing {
         v[q] = (i < topk) ? __ldg(idx_t + i) : -1;
       }
 #pragma unroll
+      for (int q = 0; q < 4; ++q) v[q] = resolve_row(*prm, seq, v[q]);  // pool row or -1
+#pragma unroll
       for (int q = 0; q < 4; ++q) {
-        const bool ok = (v[q] >= 0) && (v[q] < s_kv);
+        const bool ok = v[q] >= 0;
         const uint32_t m = __ballot_sync(0xffffffffu, ok);
         if (ok) ring[(tail + __popc(m & ((1u << lane) - 1u))) & (kIdxRing - 1)] = v[q];
         tail += __popc(m);
@@ -361,7 +365,7 @@ __device__ void index_compactor(const Ctx& c, const FwdParams& p) {
   uint32_t b = 0;
   bool ok = true;
   while (ok && it.next(pc)) {
-    ir.reset((int*)(c.smem + Y::OffRing), p.indices + (size_t)pc.t * p.topk, p.topk, p.s_kv);
+    ir.reset((int*)(c.smem + Y::OffRing), p, pc.t);
     for (int jb = 0; jb < pc.lb1; ++jb) {
       const int cnt = ir.fill(c.lane);
       if (jb >= pc.lb0) {

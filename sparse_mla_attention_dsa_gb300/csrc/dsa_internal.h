@@ -34,6 +34,16 @@ constexpr WorkspaceLayout workspace_layout(int s_q, int h_q, int npairs) {
   return L;
 }
 
+// Paged KV cache ("Flash Attention Infer算子性能优化", section "优化Paged Attention路径"):
+// indices are logical positions of the token's sequence, reached through a
+// block table of physical pages of the row pool.  block_table == nullptr means
+// the flat layout (indices are pool rows).
+struct PagedView {
+  const int32_t* block_table;   // [n_seq, max_pages] physical page of each logical page, < 0 = unmapped
+  const int32_t* seq_of_token;  // [s_q] sequence of each query token
+  int page_size, max_pages, n_seq;
+};
+
 // Everything a forward launch needs (device pointers).
 struct FwdParams {
   const uint16_t* q;         // bf16 bits [s_q, h_q, 576]
@@ -49,7 +59,31 @@ struct FwdParams {
   float* part_lse;           // [2 * npairs, h_q]
   float* part_o;             // [2 * npairs, h_q, 512]
   int npairs;
+  PagedView pg;
 };
+
+#ifdef __CUDACC__
+// Sequence of token t for the paged layout (-1 when outside [0, n_seq)); 0 for the flat layout.
+__device__ __forceinline__ int token_seq(const FwdParams& p, int t) {
+  if (p.pg.block_table == nullptr) return 0;
+  const int s = __ldg(p.pg.seq_of_token + t);
+  return (s >= 0 && s < p.pg.n_seq) ? s : -1;
+}
+
+// Pool row of index v of a token of sequence `seq`, or -1 when v names no row: outside [0, s_kv) in the
+// flat layout; negative, past the block table, on an unmapped page, in an unknown sequence or outside the
+// pool in the paged layout (row = table[seq][v / page_size] * page_size + v % page_size).
+__device__ __forceinline__ int resolve_row(const FwdParams& p, int seq, int v) {
+  if (p.pg.block_table == nullptr) return (v >= 0 && v < p.s_kv) ? v : -1;
+  if (v < 0 || seq < 0) return -1;
+  const int lp = v / p.pg.page_size;
+  if (lp >= p.pg.max_pages) return -1;
+  const int ph = __ldg(p.pg.block_table + (size_t)seq * p.pg.max_pages + lp);
+  if (ph < 0) return -1;
+  const long long row = (long long)ph * p.pg.page_size + (v - lp * p.pg.page_size);
+  return row < (long long)p.s_kv ? (int)row : -1;
+}
+#endif
 
 // Wait limit for every bounded wait inside the kernels.
 constexpr unsigned long long kWaitLimitNs = 4000000000ull;  // 4 s

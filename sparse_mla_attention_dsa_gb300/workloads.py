@@ -250,3 +250,62 @@ def small_random(seed: int, s_q: int, h_q: int, s_kv: int, topk: int, kv_format:
     idx = np.stack(rows) if rows else np.zeros((0, topk), np.int64)
     return Workload(f"small_{s_q}x{h_q}x{s_kv}x{topk}", q, kv, torch.from_numpy(idx.astype(np.int32)),
                     1.0 / math.sqrt(D_QK), kv_format)
+
+
+def _paged(name: str, q: torch.Tensor, kv_pool: torch.Tensor, indices: np.ndarray, seq_of_token: np.ndarray,
+           block_table: np.ndarray, page_size: int, kv_format: str, **meta) -> Workload:
+    return Workload(name, q, kv_pool, torch.from_numpy(indices.astype(np.int32)), 1.0 / math.sqrt(D_QK), kv_format,
+                    meta={"paged": True, "seq_of_token": torch.from_numpy(seq_of_token.astype(np.int32)),
+                          "block_table": torch.from_numpy(block_table.astype(np.int32)), "page_size": page_size,
+                          **meta})
+
+
+def small_paged(seed: int, s_q: int, h_q: int, n_seq: int, max_pages: int, page_size: int, topk: int,
+                kv_format: str = "bf16", spare_pages: int = 3, unmapped_frac: float = 0.0, invalid_frac: float = 0.0,
+                past_end: int = 0) -> Workload:
+    """A paged-cache case for parity tests.
+
+    The pool holds n_seq * max_pages + spare_pages pages in random order; sequence s's table lists a random
+    set of them, with round(unmapped_frac * max_pages) entries per sequence set to -1 (unmapped).  Each token
+    belongs to a uniform random sequence and draws `topk` distinct logical positions from [0, max_pages *
+    page_size); then round(invalid_frac * topk) slots become -1 and `past_end` slots point past the table.
+    """
+    rng = np.random.Generator(np.random.PCG64(seed))
+    n_pages = n_seq * max_pages + spare_pages
+    q = _normal_bf16(rng, (s_q, h_q, D_QK))
+    kv = _normal_bf16(rng, (n_pages * page_size, D_QK)) if kv_format == "bf16" else _fp8_kv(rng, n_pages * page_size)
+    table = rng.permutation(n_pages)[: n_seq * max_pages].reshape(n_seq, max_pages).astype(np.int64)
+    n_unmapped = int(round(unmapped_frac * max_pages))
+    for s in range(n_seq):
+        if n_unmapped:
+            table[s, rng.choice(max_pages, size=n_unmapped, replace=False)] = -1
+    seq = rng.integers(0, n_seq, size=s_q)
+    span = max_pages * page_size
+    rows = []
+    for _ in range(s_q):
+        row = _distinct(rng, 0, span, topk) if topk <= span else rng.integers(0, span, size=topk).astype(np.int64)
+        if invalid_frac > 0:
+            row[rng.choice(topk, size=int(round(invalid_frac * topk)), replace=False)] = -1
+        if past_end > 0:
+            row[rng.choice(topk, size=past_end, replace=False)] = span + rng.integers(0, 4 * page_size, size=past_end)
+        rows.append(row)
+    return _paged(f"paged_{s_q}x{h_q}x{n_seq}x{max_pages}x{page_size}", q, kv, np.stack(rows), seq, table, page_size,
+                  kv_format)
+
+
+def decode_paged(seed: int = 5, n_seq: int = 64, h_q: int = 64, s_kv_per_seq: int = 32768, topk: int = 2048,
+                 page_size: int = 64) -> Workload:
+    """decode_bf16's shape over a paged pool: n_seq sequences x 1 query token, each sequence's s_kv_per_seq
+    rows in pages of `page_size` rows scattered over the pool by a random permutation; token b attends to
+    `topk` distinct uniform logical positions of sequence b."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    max_pages = s_kv_per_seq // page_size
+    q = _normal_bf16(rng, (n_seq, h_q, D_QK))
+    kv = _normal_bf16(rng, (n_seq * s_kv_per_seq, D_QK))
+    table = rng.permutation(n_seq * max_pages).reshape(n_seq, max_pages)
+    idx = np.stack([_distinct(rng, 0, s_kv_per_seq, topk) for _ in range(n_seq)])
+    return _paged("decode_paged", q, kv, idx, np.arange(n_seq), table, page_size, "bf16", n_seq=n_seq,
+                  s_kv_per_seq=s_kv_per_seq)
+
+
+WORKLOADS["decode_paged"] = decode_paged

@@ -28,6 +28,25 @@ def oracle(wl, tokens=None):
     return O.sparse_mla_fwd_sampled(bits(wl.q), kv_raw(wl), wl.kv_format, wl.indices.numpy(), wl.sm_scale, tokens)
 
 
+def oracle_paged(wl, tokens=None):
+    """The definition over a paged workload: logical positions -> pool rows by the oracle's own translation."""
+    from oracle import paged as PG
+    tokens = list(range(wl.s_q)) if tokens is None else list(tokens)
+    rows = PG.logical_to_rows(wl.indices.numpy(), wl.meta["seq_of_token"].numpy(), wl.meta["block_table"].numpy(),
+                              wl.meta["page_size"], wl.kv.shape[0])
+    return O.sparse_mla_fwd_sampled(bits(wl.q), kv_raw(wl), wl.kv_format, rows, wl.sm_scale, tokens)
+
+
+def run_gpu_paged(wl, device="cuda"):
+    from sparse_mla_attention_dsa_gb300 import api
+    fmt = api.KV_BF16 if wl.kv_format == "bf16" else api.KV_FP8
+    out, lse = api.dsa_sparse_attn_fwd_paged(wl.q.to(device), wl.kv.to(device), wl.indices.to(device),
+                                             wl.meta["seq_of_token"].to(device), wl.meta["block_table"].to(device),
+                                             wl.meta["page_size"], wl.sm_scale, kv_format=fmt, check_status=True)
+    torch.cuda.synchronize()
+    return out, lse
+
+
 def run_gpu(wl, device="cuda"):
     from sparse_mla_attention_dsa_gb300 import api
     q = wl.q.to(device)
