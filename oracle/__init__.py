@@ -11,8 +11,8 @@ Modules:
               gather, full (non-online) softmax, weighted sum, lse.
   emu         the pages' blockwise online-softmax algorithm with skip-scale,
               emulated step by step in float32 with the bf16 cast of S.
-  formats     bit-level decoders of bf16 and FP8-e4m3 and of the 656-byte FP8
-              KV row.
+  formats     bit-level decoders of bf16, FP8-e4m3 and FP4-e2m1 and of the
+              656-byte FP8 and 448-byte FP4 KV rows.
   paged       logical positions of a sequence -> rows of a paged KV pool
               through a block table (the forward itself is unchanged).
 

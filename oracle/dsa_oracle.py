@@ -25,7 +25,7 @@ from __future__ import annotations
 
 import numpy as np
 
-from .formats import bf16_bits_to_f64, fp8_rows_to_f64
+from .formats import bf16_bits_to_f64, fp4_rows_to_f64, fp8_rows_to_f64
 
 D_QK = 576
 D_V = 512
@@ -79,11 +79,13 @@ def q_to_f64(q_bits: np.ndarray) -> np.ndarray:
 
 
 def kv_to_f64(kv_raw: np.ndarray, kv_format: str) -> np.ndarray:
-    """KV cache bytes -> float64 [s_kv, 576] (bf16 bits, or 656-byte FP8 rows)."""
+    """KV cache bytes -> float64 [s_kv, 576] (bf16 bits, 656-byte FP8 rows or 448-byte FP4 rows)."""
     if kv_format == "bf16":
         return bf16_bits_to_f64(kv_raw)
     if kv_format == "fp8":
         return fp8_rows_to_f64(kv_raw)
+    if kv_format == "fp4":
+        return fp4_rows_to_f64(kv_raw)
     raise ValueError(kv_format)
 
 

@@ -50,10 +50,10 @@ class Workload:
 
     name: str
     q: torch.Tensor  # bf16 [s_q, h_q, 576]
-    kv: torch.Tensor  # bf16 [s_kv, 576]  or  uint8 [s_kv, 656] (fp8 rows)
+    kv: torch.Tensor  # bf16 [s_kv, 576]  or  uint8 [s_kv, 656] (fp8 rows)  or  uint8 [s_kv, 448] (fp4 rows)
     indices: torch.Tensor  # int32 [s_q, topk]
     sm_scale: float
-    kv_format: str  # "bf16" or "fp8"
+    kv_format: str  # "bf16", "fp8" or "fp4"
     meta: dict = field(default_factory=dict)
 
     @property
@@ -110,6 +110,40 @@ def _fp8_kv(rng: np.random.Generator, s_kv: int, chunk_rows: int = 1 << 18) -> t
         lat = torch.from_numpy(rng.standard_normal((r1 - r0, D_V), dtype=np.float32))
         rope = torch.from_numpy(rng.standard_normal((r1 - r0, D_ROPE), dtype=np.float32)).to(torch.bfloat16)
         rows[r0:r1] = quantize_fp8_rows(lat, rope)
+    return rows
+
+
+FP4_GROUP = 32
+FP4_ROW_BYTES = 448
+_E2M1_GRID = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0], dtype=np.float32)
+
+
+def quantize_fp4_rows(latent: np.ndarray, rope_bf16: torch.Tensor) -> torch.Tensor:
+    """Pack float32 latents [n, 512] and bf16 rope [n, 64] into 448-byte FP4 rows: 512 e2m1 codes two per
+    byte (low nibble = even channel), 16 float32 scales (max |x| / 6 per 32 channels, 1 for an all-zero
+    group), 64 bf16 rope values.  Codes are the nearest e2m1 magnitude, ties to the even code."""
+    n = latent.shape[0]
+    g = latent.astype(np.float32).reshape(n, D_V // FP4_GROUP, FP4_GROUP)
+    amax = np.abs(g).max(axis=2)
+    scale = np.where(amax > 0, amax / np.float32(6.0), np.float32(1.0)).astype(np.float32)
+    y = np.abs(g) / scale[:, :, None]
+    d = np.abs(y[..., None] - _E2M1_GRID) + (np.arange(8) & 1) * np.float32(1e-6)  # ties -> even code
+    mag = d.argmin(axis=-1).astype(np.uint8)
+    codes = (mag | np.where(g < 0, 8, 0).astype(np.uint8)).reshape(n, D_V)
+    rows = np.empty((n, FP4_ROW_BYTES), dtype=np.uint8)
+    rows[:, :D_V // 2] = codes[:, 0::2] | (codes[:, 1::2] << 4)
+    rows[:, D_V // 2:D_V // 2 + 64] = scale.view(np.uint8).reshape(n, 64)
+    rows[:, D_V // 2 + 64:] = rope_bf16.contiguous().view(torch.uint8).view(n, 2 * D_ROPE).numpy()
+    return torch.from_numpy(rows)
+
+
+def _fp4_kv(rng: np.random.Generator, s_kv: int, chunk_rows: int = 1 << 17) -> torch.Tensor:
+    rows = torch.empty((s_kv, FP4_ROW_BYTES), dtype=torch.uint8)
+    for r0 in range(0, s_kv, chunk_rows):
+        r1 = min(s_kv, r0 + chunk_rows)
+        lat = rng.standard_normal((r1 - r0, D_V), dtype=np.float32)
+        rope = torch.from_numpy(rng.standard_normal((r1 - r0, D_ROPE), dtype=np.float32)).to(torch.bfloat16)
+        rows[r0:r1] = quantize_fp4_rows(lat, rope)
     return rows
 
 
@@ -237,7 +271,8 @@ def small_random(seed: int, s_q: int, h_q: int, s_kv: int, topk: int, kv_format:
     """A generic small case for parity tests (any shape, optional -1 slots)."""
     rng = np.random.Generator(np.random.PCG64(seed))
     q = _normal_bf16(rng, (s_q, h_q, D_QK), sigma=q_sigma)
-    kv = _normal_bf16(rng, (s_kv, D_QK)) if kv_format == "bf16" else _fp8_kv(rng, s_kv)
+    kv = {"bf16": lambda: _normal_bf16(rng, (s_kv, D_QK)), "fp8": lambda: _fp8_kv(rng, s_kv),
+          "fp4": lambda: _fp4_kv(rng, s_kv)}[kv_format]()
     rows = []
     for _ in range(s_q):
         if distinct and topk <= s_kv:
@@ -308,4 +343,16 @@ def decode_paged(seed: int = 5, n_seq: int = 64, h_q: int = 64, s_kv_per_seq: in
                   s_kv_per_seq=s_kv_per_seq)
 
 
+def decode_fp4(seed: int = 6, n_seq: int = 128, h_q: int = 128, s_kv_per_seq: int = 65536, topk: int = 2048,
+               q_sigma: float = 2.0) -> Workload:
+    """decode_fp8's shape over an FP4 cache (448-byte rows): n_seq sequences x 1 token, Q ~ N(0, sigma=2)."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    q = _normal_bf16(rng, (n_seq, h_q, D_QK), sigma=q_sigma)
+    kv = _fp4_kv(rng, n_seq * s_kv_per_seq)
+    idx = np.stack([_distinct(rng, 0, s_kv_per_seq, topk) + b * s_kv_per_seq for b in range(n_seq)])
+    return Workload("decode_fp4", q, kv, torch.from_numpy(idx.astype(np.int32)), 1.0 / math.sqrt(D_QK), "fp4",
+                    meta={"n_seq": n_seq, "s_kv_per_seq": s_kv_per_seq, "q_sigma": q_sigma})
+
+
 WORKLOADS["decode_paged"] = decode_paged
+WORKLOADS["decode_fp4"] = decode_fp4
