@@ -50,7 +50,7 @@ def _flops(indices: torch.Tensor, s_kv: int, h_q: int) -> float:
 def _alg_bytes(wl) -> float:
     """Algorithmic bytes of one forward: gathered KV rows + Q + out + lse + indices."""
     nv = ((wl.indices >= 0) & (wl.indices < wl.s_kv)).sum().item()
-    row = 1152 if wl.kv_format == "bf16" else 656
+    row = {"bf16": 1152, "fp8": 656, "fp4": 448}[wl.kv_format]
     return nv * row + wl.s_q * wl.h_q * (576 * 2 + 512 * 2 + 4) + wl.indices.numel() * 4
 
 
@@ -102,7 +102,7 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows)}
 
 
-KERNEL_SOURCES = ("dsa_fwd_impl.cuh", "ptx.cuh", "dsa_internal.h", "dsa_fwd.cu", "dsa_fwd_fp8.cu")
+KERNEL_SOURCES = ("dsa_fwd_impl.cuh", "ptx.cuh", "dsa_internal.h", "dsa_fwd.cu", "dsa_fwd_fp8.cu", "dsa_fwd_fp4.cu")
 
 
 def _kernel_sources_sha256() -> str:
@@ -199,11 +199,13 @@ def run_gb300(args, rank: int, world: int, local_rank: int):
     else:
         wl = W.WORKLOADS[args.workload]()
     flops = _flops(wl.indices, wl.s_kv, wl.h_q)
-    fwd = api.dsa_sparse_attn_fwd if wl.kv_format == "bf16" else api.dsa_sparse_attn_fwd_fp8kv
+    fwd = {"bf16": api.dsa_sparse_attn_fwd, "fp8": api.dsa_sparse_attn_fwd_fp8kv,
+           "fp4": api.dsa_sparse_attn_fwd_fp4kv}[wl.kv_format]
+    fmt = {"bf16": api.KV_BF16, "fp8": api.KV_FP8, "fp4": api.KV_FP4}[wl.kv_format]
     q, kv, idx = wl.q.to(dev), wl.kv.to(dev), wl.indices.to(dev)
     out = torch.empty((wl.s_q, wl.h_q, 512), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((wl.s_q, wl.h_q), dtype=torch.float32, device=dev)
-    ws = torch.empty(api.dsa_sparse_attn_fwd_workspace_size(wl.s_q, wl.h_q, wl.topk, 0 if wl.kv_format == "bf16" else 1),
+    ws = torch.empty(api.dsa_sparse_attn_fwd_workspace_size(wl.s_q, wl.h_q, wl.topk, fmt),
                      dtype=torch.uint8, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
@@ -318,7 +320,7 @@ def _report(args, wl, flops, ms, kms, e2e_ms, clocks, world):
     if args.s_q is not None and args.workload == "prefill_causal" and args.s_q != 4096 and args.traffic is None:
         traffic = None  # the recorded capture is of the full-size workload
     roof.update({"traffic": traffic, "alg_bytes": abytes, "alg_flops": flops, "peak_source": peak_src,
-                 "kernel": "dsa_fwd_kernel<%s>" % ("false" if wl.kv_format == "bf16" else "true"),
+                 "kernel": "dsa_fwd_kernel<%d>" % {"bf16": 0, "fp8": 1, "fp4": 2}[wl.kv_format],
                  "kernel_ms": kms, "tensor_frac": tf_achieved / peak_tf, "hbm_frac": gbs_achieved / hbm_gbs,
                  "roofline_ms": 1e3 * max(t_flops, t_bytes)})
     value = world * flops / (ms * 1e-3) / 1e12
@@ -356,7 +358,8 @@ def main():
     ap.add_argument("--s-q", type=int, default=4096, help="query tokens (4096 = the benchmark workload)")
     ap.add_argument("--skip-e2e", action="store_true")
     ap.add_argument("--workload", default="prefill_causal",
-                    choices=["prefill_causal", "decode_bf16", "decode_fp8", "long_prefill", "decode_paged", "tiny"])
+                    choices=["prefill_causal", "decode_bf16", "decode_fp8", "long_prefill", "decode_paged",
+                             "decode_fp4", "tiny"])
     ap.add_argument("--traffic", type=float, default=None,
                     help="DRAM bytes per attention-kernel launch from an ncu capture (null when not given)")
     args = ap.parse_args()

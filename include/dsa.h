@@ -35,6 +35,11 @@
  *                  bytes   0..511  e4m3 latent channels 0..511
  *                  bytes 512..527  4 x float32 scale, scale g applies to channels 128g..128g+127
  *                  bytes 528..655  64 x bf16 rope channels 512..575
+ *            uint8 [s_kv, 448] FP4 rows                 (dsa_sparse_attn_fwd_fp4kv):
+ *                  bytes   0..255  e2m1 latent codes, two per byte: byte i holds channel 2i in its
+ *                                  low nibble and channel 2i+1 in its high nibble
+ *                  bytes 256..319  16 x float32 scale, scale g applies to channels 32g..32g+31
+ *                  bytes 320..447  64 x bf16 rope channels 512..575
  *   indices  int32 [s_q, topk]   global row ids into kv
  *   out      bf16  [s_q, h_q, 512]
  *   lse      fp32  [s_q, h_q]    natural-log log-sum-exp of the scaled logits
@@ -62,6 +67,7 @@ extern "C" {
 #define DSA_D_V 512
 #define DSA_D_ROPE 64
 #define DSA_FP8_ROW_BYTES 656
+#define DSA_FP4_ROW_BYTES 448
 #define DSA_MAX_HEADS 128
 #define DSA_B_TOPK 128
 
@@ -75,7 +81,7 @@ typedef enum {
   DSA_ERR_WORKSPACE = 6       /* workspace null or smaller than dsa_sparse_attn_fwd_workspace_size() */
 } dsa_status;
 
-typedef enum { DSA_KV_BF16 = 0, DSA_KV_FP8 = 1 } dsa_kv_format;
+typedef enum { DSA_KV_BF16 = 0, DSA_KV_FP8 = 1, DSA_KV_FP4 = 2 } dsa_kv_format;
 
 /* Bytes of device workspace a forward call with these shapes needs on the
  * current device (scheduler metadata, per-piece partial outputs for tokens
@@ -131,7 +137,8 @@ DSA_API dsa_status dsa_sparse_attn_fwd_noalloc(const void* q, const void* kv, co
 /* The forward over a paged KV cache ("Flash Attention Infer算子性能优化", section
  * "优化Paged Attention路径": a sequence's KV lives in fixed-size pages of a shared
  * pool and is reached through a block table).
- *   kv_format     DSA_KV_BF16 (kv_pool bf16 [n_rows, 576]) or DSA_KV_FP8 (uint8 [n_rows, 656]);
+ *   kv_format     DSA_KV_BF16 (kv_pool bf16 [n_rows, 576]), DSA_KV_FP8 (uint8 [n_rows, 656]) or
+ *                 DSA_KV_FP4 (uint8 [n_rows, 448]);
  *                 the pool holds n_rows / page_size pages of page_size rows, page k at rows
  *                 [k * page_size, (k + 1) * page_size).
  *   indices       int32 [s_q, topk]: logical positions in the token's own sequence.
@@ -150,6 +157,17 @@ DSA_API dsa_status dsa_sparse_attn_fwd_paged(int kv_format, const void* q, const
                                              int h_q, int n_rows, int topk, int n_seq, int max_pages, int page_size,
                                              float sm_scale, void* out, float* lse, void* workspace,
                                              size_t workspace_bytes, cudaStream_t stream);
+
+/* The forward with an FP4 (e2m1) KV cache of 448-byte rows (layout above).  The
+ * page's "能不能用 1C1V" section names FP4 beside FP8 as a decoding KV format but
+ * gives no layout: the row is this library's reading (the FP8 row's pattern with
+ * 4-bit codes and one scale per 32 channels).  Latent channels are dequantised as
+ * e2m1 * scale and rounded to bf16 before the tensor cores, as for FP8.  Arguments
+ * as for dsa_sparse_attn_fwd, with kv = uint8 [s_kv, 448]; the workspace size is
+ * dsa_sparse_attn_fwd_workspace_size(..., DSA_KV_FP4). */
+DSA_API dsa_status dsa_sparse_attn_fwd_fp4kv(const void* q, const void* kv_fp4, const int32_t* indices, int s_q, int h_q,
+                                             int s_kv, int topk, float sm_scale, void* out, float* lse,
+                                             void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /* Synchronises `stream` and returns the device-side status a previous forward
  * call left in `workspace` (DSA_OK or DSA_ERR_DEVICE_TIMEOUT), or DSA_ERR_CUDA

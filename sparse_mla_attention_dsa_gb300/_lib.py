@@ -15,6 +15,7 @@ SIGNATURES = {
     "dsa_sparse_attn_fwd_workspace_size": (_S, [_I, _I, _I, _I]),
     "dsa_sparse_attn_fwd": (_I, [_P, _P, _P, _I, _I, _I, _I, _F, _P, _P, _P, _S, _P]),
     "dsa_sparse_attn_fwd_fp8kv": (_I, [_P, _P, _P, _I, _I, _I, _I, _F, _P, _P, _P, _S, _P]),
+    "dsa_sparse_attn_fwd_fp4kv": (_I, [_P, _P, _P, _I, _I, _I, _I, _F, _P, _P, _P, _S, _P]),
     "dsa_read_device_status": (_I, [_P, _P]),
     "dsa_status_string": (ctypes.c_char_p, [_I]),
     "dsa_kernels_per_call": (_I, []),

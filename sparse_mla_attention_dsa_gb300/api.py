@@ -18,6 +18,8 @@ D_V = 512
 FP8_ROW_BYTES = 656
 KV_BF16 = 0
 KV_FP8 = 1
+KV_FP4 = 2
+FP4_ROW_BYTES = 448
 
 
 def _ptr(t):
@@ -42,8 +44,9 @@ def _check(q, kv, indices, kv_format):
         if kv.dtype != torch.bfloat16 or kv.dim() != 2 or kv.shape[1] != D_QK or not kv.is_contiguous():
             raise ValueError("kv must be a contiguous bf16 tensor [s_kv, 576]")
     else:
-        if kv.dtype != torch.uint8 or kv.dim() != 2 or kv.shape[1] != FP8_ROW_BYTES or not kv.is_contiguous():
-            raise ValueError("kv must be a contiguous uint8 tensor [s_kv, 656] of FP8 rows")
+        nb = FP8_ROW_BYTES if kv_format == KV_FP8 else FP4_ROW_BYTES
+        if kv.dtype != torch.uint8 or kv.dim() != 2 or kv.shape[1] != nb or not kv.is_contiguous():
+            raise ValueError(f"kv must be a contiguous uint8 tensor [s_kv, {nb}] of quantised rows")
     if indices.dtype != torch.int32 or indices.dim() != 2 or indices.shape[0] != q.shape[0] or not indices.is_contiguous():
         raise ValueError("indices must be a contiguous int32 tensor [s_q, topk]")
 
@@ -117,6 +120,13 @@ def dsa_sparse_attn_fwd_paged(q, kv_pool, indices, seq_of_token, block_table, pa
     if check_status:
         dsa_read_device_status(workspace, stream)
     return out, lse
+
+
+def dsa_sparse_attn_fwd_fp4kv(q, kv_fp4, indices, sm_scale, out=None, lse=None, workspace=None, stream=None,
+                              check_status=False):
+    """Sparse MLA forward with an FP4 (e2m1) KV cache of 448-byte rows."""
+    return _forward("dsa_sparse_attn_fwd_fp4kv", KV_FP4, q, kv_fp4, indices, sm_scale, out, lse, workspace, stream,
+                    check_status)
 
 
 def dsa_read_device_status(workspace, stream=None) -> int:

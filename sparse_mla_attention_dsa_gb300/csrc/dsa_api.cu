@@ -16,6 +16,8 @@ int fwd_max_active_pairs();
 cudaError_t launch_fwd_bf16(const FwdParams& p, cudaStream_t stream);
 int fwd_fp8_max_active_pairs();
 cudaError_t launch_fwd_fp8(const FwdParams& p, cudaStream_t stream);
+int fwd_fp4_max_active_pairs();
+cudaError_t launch_fwd_fp4(const FwdParams& p, cudaStream_t stream);
 
 // ----------------------------------------------------------------------------
 // Scheduling: n_valid per token, then (by the last CTA to finish) the prefix
@@ -206,7 +208,9 @@ static bool device_ok() {
 }
 
 static int pairs_for(int kv_format) {
-  return kv_format == DSA_KV_FP8 ? fwd_fp8_max_active_pairs() : fwd_max_active_pairs();
+  return kv_format == DSA_KV_FP8 ? fwd_fp8_max_active_pairs()
+         : kv_format == DSA_KV_FP4 ? fwd_fp4_max_active_pairs()
+                                   : fwd_max_active_pairs();
 }
 
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -262,7 +266,9 @@ static dsa_status forward(int kv_format, const void* q, const void* kv, const in
   cudaError_t e;
   const bool timed = g_ev_before != nullptr && g_ev_after != nullptr;
   if (timed) cudaEventRecord(g_ev_before, stream);
-  e = (kv_format == DSA_KV_BF16) ? launch_fwd_bf16(p, stream) : launch_fwd_fp8(p, stream);
+  e = (kv_format == DSA_KV_BF16)  ? launch_fwd_bf16(p, stream)
+      : (kv_format == DSA_KV_FP8) ? launch_fwd_fp8(p, stream)
+                                  : launch_fwd_fp4(p, stream);
   if (timed) cudaEventRecord(g_ev_after, stream);
   if (e != cudaSuccess) return DSA_ERR_CUDA;
   const dim3 cgrid((unsigned)npairs, (unsigned)((h_q + kCombineWarps - 1) / kCombineWarps));
@@ -277,7 +283,7 @@ extern "C" {
 
 size_t dsa_sparse_attn_fwd_workspace_size(int s_q, int h_q, int topk, int kv_format) {
   if (s_q < 0 || h_q < 1 || h_q > dsa::kMaxHeads || topk < 1) return 0;
-  if (kv_format != DSA_KV_BF16 && kv_format != DSA_KV_FP8) return 0;
+  if (kv_format != DSA_KV_BF16 && kv_format != DSA_KV_FP8 && kv_format != DSA_KV_FP4) return 0;
   const int npairs = dsa::pairs_for(kv_format);
   if (npairs <= 0) return 0;
   return dsa::workspace_layout(s_q, h_q, npairs).total;
@@ -302,7 +308,7 @@ dsa_status dsa_sparse_attn_fwd_paged(int kv_format, const void* q, const void* k
                                      int n_rows, int topk, int n_seq, int max_pages, int page_size, float sm_scale,
                                      void* out, float* lse, void* workspace, size_t workspace_bytes,
                                      cudaStream_t stream) {
-  if (kv_format != DSA_KV_BF16 && kv_format != DSA_KV_FP8) return DSA_ERR_INVALID_ARG;
+  if (kv_format != DSA_KV_BF16 && kv_format != DSA_KV_FP8 && kv_format != DSA_KV_FP4) return DSA_ERR_INVALID_ARG;
   if (n_seq < 1 || max_pages < 1 || page_size < 1 || (long long)n_seq * max_pages > 0x7fffffffLL)
     return DSA_ERR_INVALID_ARG;
   if (s_q > 0 && (!seq_of_token || !block_table)) return DSA_ERR_INVALID_ARG;
@@ -311,6 +317,13 @@ dsa_status dsa_sparse_attn_fwd_paged(int kv_format, const void* q, const void* k
   const dsa::PagedView pg{block_table, seq_of_token, page_size, max_pages, n_seq};
   return dsa::forward(kv_format, q, kv_pool, indices, s_q, h_q, n_rows, topk, sm_scale, out, lse, workspace,
                       workspace_bytes, stream, &pg);
+}
+
+dsa_status dsa_sparse_attn_fwd_fp4kv(const void* q, const void* kv_fp4, const int32_t* indices, int s_q, int h_q,
+                                     int s_kv, int topk, float sm_scale, void* out, float* lse, void* workspace,
+                                     size_t workspace_bytes, cudaStream_t stream) {
+  return dsa::forward(DSA_KV_FP4, q, kv_fp4, indices, s_q, h_q, s_kv, topk, sm_scale, out, lse, workspace,
+                      workspace_bytes, stream);
 }
 
 dsa_status dsa_read_device_status(const void* workspace, cudaStream_t stream) {

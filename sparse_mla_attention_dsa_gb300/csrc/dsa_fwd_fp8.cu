@@ -3,6 +3,6 @@
 #include "dsa_fwd_impl.cuh"
 
 namespace dsa {
-int fwd_fp8_max_active_pairs() { return max_active_pairs_impl<true>(); }
-cudaError_t launch_fwd_fp8(const FwdParams& p, cudaStream_t stream) { return launch_impl<true>(p, stream); }
+int fwd_fp8_max_active_pairs() { return max_active_pairs_impl<fwd::kFmtFp8>(); }
+cudaError_t launch_fwd_fp8(const FwdParams& p, cudaStream_t stream) { return launch_impl<fwd::kFmtFp8>(p, stream); }
 }  // namespace dsa

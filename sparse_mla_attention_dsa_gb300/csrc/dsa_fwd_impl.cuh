@@ -41,6 +41,7 @@
 // ingests random 128-byte row pieces at only a few tens of bytes per clock.
 #pragma once
 #include <cuda_fp16.h>
+#include <cuda_fp4.h>
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
@@ -50,6 +51,10 @@
 namespace dsa {
 
 namespace fwd {
+
+// KV formats of the kernel template: bf16 rows, or quantised rows (FP8 / FP4) that are staged raw and
+// dequantised to bf16 before the tensor cores.
+constexpr int kFmtBf16 = 0, kFmtFp8 = 1, kFmtFp4 = 2;
 
 constexpr int kThreads = 512;
 constexpr int kSoftmaxWarps = 8;                 // QK side, warps 4..11
@@ -96,23 +101,39 @@ __device__ __forceinline__ void cp_async_unit(uint32_t dst, const uint8_t* kv, c
 // FP8 rows: raw units staged before dequantisation
 constexpr int kRawSlots = 4;
 constexpr int kRawASlot = 128 * 64;              // QK side unit: 128 rows x 64 bytes (64 e4m3 or 32 bf16)
-constexpr int kRawBRowBytes = 528;               // PV side: first 528 bytes of a row (512 e4m3 + 4 fp32 scales)
-constexpr int kRawBSlot = kVGroupRows * kRawBRowBytes;
-constexpr int kScaleSlot = 128 * 16;             // QK side: 4 fp32 scales of each of 128 rows
+// Quantised rows: [latent codes | fp32 scales | 64 bf16 rope]
+//   FP8: 512 e4m3 (512 B) | 4 scales, one per 128 channels (16 B) | rope (128 B) = 656 B
+//   FP4: 512 e2m1 two per byte, low nibble = even channel (256 B) | 16 scales, one per 32 channels (64 B) |
+//        rope (128 B) = 448 B
+template <int kFmt>
+struct QRow {
+  static constexpr bool kF4 = kFmt == 2;
+  static constexpr int kBytes = kF4 ? 448 : 656;
+  static constexpr int kScaleOff = kF4 ? 256 : 512;     // = latent code bytes
+  static constexpr int kScaleBytes = kF4 ? 64 : 16;
+  static constexpr int kRopeOff = kScaleOff + kScaleBytes;
+  static constexpr int kLatUnits = kF4 ? 4 : 8;         // QK raw units of 64 code bytes per row: 128 | 64 channels
+  static constexpr int kUnits = kLatUnits + 2;           // + the two 64-byte rope halves
+  static constexpr int kRawBRow = kRopeOff;              // PV side stages codes + scales of each row
+  static constexpr int kRawBSlot = kVGroupRows * kRawBRow;
+  static constexpr int kScaleSlot = 128 * kScaleBytes;   // QK side: the scales of each of 128 rows
+};
 
 __host__ __device__ constexpr int align1k(int x) { return (x + 1023) / 1024 * 1024; }
 
 // Shared-memory layout of each side for one KV format.
-template <bool kFp8>
+template <int kFmt>
 struct Lay {
-  static constexpr int kKSlots = kFp8 ? 6 : 0;   // FP8: ring of 128-row x 64-column chunks
-  static constexpr int kVSlots = kFp8 ? 7 : 9;
+  static constexpr bool kQuant = kFmt != kFmtBf16;
+  using R = QRow<kFmt == kFmtBf16 ? kFmtFp8 : kFmt>;
+  static constexpr int kKSlots = kQuant ? 6 : 0;   // FP8: ring of 128-row x 64-column chunks
+  static constexpr int kVSlots = kQuant ? 7 : 9;
   // QK side (cluster rank 0).  bf16: latent halves [2][8 groups][8 atoms], then rope atoms [2][8 groups].
   static constexpr int A_OffK = 0;
-  static constexpr int A_OffKR = A_OffK + (kFp8 ? 0 : 2 * kHalfLatBytes);
-  static constexpr int A_OffRaw = kFp8 ? A_OffK + kKSlots * kKChunkBytes : A_OffKR + 2 * kHalfRopeBytes;
-  static constexpr int A_OffScales = A_OffRaw + (kFp8 ? kRawSlots * kRawASlot : 0);
-  static constexpr int A_OffQRope = A_OffScales + (kFp8 ? 2 * kScaleSlot : 0);
+  static constexpr int A_OffKR = A_OffK + (kQuant ? 0 : 2 * kHalfLatBytes);
+  static constexpr int A_OffRaw = kQuant ? A_OffK + kKSlots * kKChunkBytes : A_OffKR + 2 * kHalfRopeBytes;
+  static constexpr int A_OffScales = A_OffRaw + (kQuant ? kRawSlots * kRawASlot : 0);
+  static constexpr int A_OffQRope = A_OffScales + (kQuant ? 2 * R::kScaleSlot : 0);
   static constexpr int A_OffMsg = align1k(A_OffQRope + kKChunkBytes);  // one outgoing message buffer
   static constexpr int A_OffMax = A_OffMsg + kMsgSlot;  // [2 halves][128] float
   static constexpr int A_OffSe = A_OffMax + 2 * 128 * 4;
@@ -120,7 +141,7 @@ struct Lay {
   // PV side (cluster rank 1)
   static constexpr int B_OffV = 0;
   static constexpr int B_OffRaw = B_OffV + kVSlots * kVGroupBytes;
-  static constexpr int B_OffMsg = align1k(B_OffRaw + (kFp8 ? kRawSlots * kRawBSlot : 0));
+  static constexpr int B_OffMsg = align1k(B_OffRaw + (kQuant ? kRawSlots * R::kRawBSlot : 0));
   static constexpr int B_End = B_OffMsg + 2 * kMsgSlot;
   // common tail: compaction ring, per-block index lists, barriers, misc
   static constexpr int OffCommon = (A_End > B_End ? A_End : B_End);
@@ -274,6 +295,24 @@ __device__ __forceinline__ void dequant16(const uint4 w, float scale, uint4& o0,
   o1 = make_uint4(out[4], out[5], out[6], out[7]);
 }
 
+// 32 e2m1 codes (one 16-byte piece; byte i holds channel 2i in its low nibble and 2i + 1 in its high
+// nibble) times `scale`, rounded to bf16: four 16-byte pieces of 8 bf16 each, channel order kept.
+__device__ __forceinline__ void dequant32_fp4(const uint4 w, float scale, uint4 (&o)[4]) {
+  const uint32_t in[4] = {w.x, w.y, w.z, w.w};
+  uint32_t out[16];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const __half2_raw h = __nv_cvt_fp4x2_to_halfraw2((__nv_fp4x2_storage_t)((in[i] >> (8 * j)) & 0xFFu), __NV_E2M1);
+      const float2 f = __half22float2(__half2(h));
+      out[4 * i + j] = pack_bf16x2(f.x * scale, f.y * scale);
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < 4; ++k) o[k] = make_uint4(out[4 * k], out[4 * k + 1], out[4 * k + 2], out[4 * k + 3]);
+}
+
 struct Ctx {
   uint8_t* smem;
   uint32_t sbase, bars, tmem, rank, peer, peer_abort;
@@ -354,9 +393,9 @@ __device__ __forceinline__ uint32_t blocks_of_pair(const FwdParams& p, int pair)
 // ============================================================================ both sides: index lists
 // Warp 0: walks this pair's pieces, compacts the valid slots of each block in
 // order and publishes them (row ids + count) in a ring of kIdxSlots lists.
-template <bool kFp8>
+template <int kFmt>
 __device__ void index_compactor(const Ctx& c, const FwdParams& p) {
-  using Y = Lay<kFp8>;
+  using Y = Lay<kFmt>;
   IndexRing ir;
   int* lists = (int*)(c.smem + Y::OffIdx);
   PieceIter it;
@@ -389,9 +428,11 @@ __device__ void index_compactor(const Ctx& c, const FwdParams& p) {
 }
 
 // ============================================================================ QK side
-// FP8 rows: cp.async into a raw ring, dequantised by the same warps into the K chunk ring.
-static __device__ void qk_gather_fp8(const Ctx& c, const FwdParams& p) {
-  using Y = Lay<true>;
+// Quantised rows (FP8 / FP4): cp.async into a raw ring, dequantised by the same warps into the K chunk ring.
+template <int kFmt>
+static __device__ void qk_gather_q(const Ctx& c, const FwdParams& p) {
+  using Y = Lay<kFmt>;
+  using R = QRow<kFmt>;
   uint8_t* smem = c.smem;
   const int warp = c.warp, lane = c.lane;
   const int gw = (warp == 1) ? 0 : warp - 11;  // 0..4
@@ -401,53 +442,80 @@ static __device__ void qk_gather_fp8(const Ctx& c, const FwdParams& p) {
   const uint32_t nblk = blocks_of_pair(p, c.pair);
   bool ok = true;
   {
-    // Per block 10 raw units of 128 rows x 64 bytes: latent chunks 0..7 (e4m3) and rope halves 8..9
-    // (bf16); the block's scales ride with unit 0.  Units are staged in a 4-slot ring two units ahead,
-    // then dequantised (latent) or copied (rope) into the swizzled K chunk ring.
-    const uint32_t nunits = nblk * 10u;
+    // Per block R::kUnits raw units of 128 rows x 64 bytes: latent code units (one 64-channel chunk of
+    // e4m3, or two of e2m1) and the two rope halves (bf16); the block's scales ride with unit 0.  Units
+    // are staged in a 4-slot ring two units ahead, then dequantised (latent) or copied (rope) into the
+    // swizzled K chunk ring.
+    const uint32_t nunits = nblk * (uint32_t)R::kUnits;
     auto issue = [&](uint32_t u) -> bool {
-      const uint32_t b = u / 10u;
-      const int k = (int)(u % 10u), rs = (int)(u % kRawSlots);
+      const uint32_t b = u / (uint32_t)R::kUnits;
+      const int k = (int)(u % (uint32_t)R::kUnits), rs = (int)(u % kRawSlots);
       if (!wait(c, RAW_EMPTY + rs, ((u / kRawSlots) & 1u) ^ 1u)) return false;
       if (k == 0 && !wait(c, IDX_FULL + (int)(b % kIdxSlots), (b / kIdxSlots) & 1u)) return false;
       const int* l = lists + (int)(b % kIdxSlots) * kIdxSlotInts;
       const uint32_t dst = c.sbase + Y::A_OffRaw + (uint32_t)rs * kRawASlot;
-      const int src_off = (k < 8) ? 64 * k : 528 + 64 * (k - 8);
+      const int src_off = (k < R::kLatUnits) ? 64 * k : R::kRopeOff + 64 * (k - R::kLatUnits);
       for (int q = gt; q < 512; q += kGT)
-        cp_async16(dst + (uint32_t)q * 16u, p.kv + (size_t)l[q >> 2] * kFp8RowBytes + src_off + 16 * (q & 3));
+        cp_async16(dst + (uint32_t)q * 16u, p.kv + (size_t)l[q >> 2] * R::kBytes + src_off + 16 * (q & 3));
       if (k == 0) {
-        const uint32_t sd = c.sbase + Y::A_OffScales + (b & 1u) * kScaleSlot;
-        for (int q = gt; q < 128; q += kGT) cp_async16(sd + (uint32_t)q * 16u, p.kv + (size_t)l[q] * kFp8RowBytes + 512);
+        constexpr int kPer = R::kScaleBytes / 16;  // 16-byte pieces of scales per row
+        const uint32_t sd = c.sbase + Y::A_OffScales + (b & 1u) * R::kScaleSlot;
+        for (int q = gt; q < 128 * kPer; q += kGT)
+          cp_async16(sd + (uint32_t)q * 16u, p.kv + (size_t)l[q / kPer] * R::kBytes + R::kScaleOff + 16 * (q % kPer));
       }
       cp_async_arrive(c.bar(RAW_FULL + rs));
       return true;
     };
     auto consume = [&](uint32_t u) -> bool {
-      const uint32_t b = u / 10u;
-      const int k = (int)(u % 10u), rs = (int)(u % kRawSlots);
+      const uint32_t b = u / (uint32_t)R::kUnits;
+      const int k = (int)(u % (uint32_t)R::kUnits), rs = (int)(u % kRawSlots);
       if (!wait(c, RAW_FULL + rs, (u / kRawSlots) & 1u)) return false;
-      const uint32_t cs = b * (uint32_t)kChunksPerBlock + (uint32_t)min(k, 8);
-      const int s = (int)(cs % Y::kKSlots);
-      if (k <= 8 && !wait(c, A_K_EMPTY + s, ((cs / Y::kKSlots) & 1u) ^ 1u)) return false;
       const uint8_t* raw = smem + Y::A_OffRaw + rs * kRawASlot;
-      uint8_t* kd = smem + Y::A_OffK + s * kKChunkBytes;
-      if (k < 8) {
-        const float* sc = (const float*)(smem + Y::A_OffScales + (b & 1u) * kScaleSlot);
-        for (int q = gt; q < 512; q += kGT) {
-          const int r = q >> 2, rp = q & 3;
-          uint4 o0, o1;
-          dequant16(*(const uint4*)(raw + q * 16), sc[r * 4 + (k >> 1)], o0, o1);
-          *(uint4*)(kd + sw128_off((uint32_t)r, (uint32_t)(2 * rp))) = o0;
-          *(uint4*)(kd + sw128_off((uint32_t)r, (uint32_t)(2 * rp + 1))) = o1;
+      const float* sc = (const float*)(smem + Y::A_OffScales + (b & 1u) * R::kScaleSlot);
+      if (k < R::kLatUnits) {
+        if constexpr (!R::kF4) {  // FP8: unit k = latent chunk k
+          const uint32_t cs = b * (uint32_t)kChunksPerBlock + (uint32_t)k;
+          const int s = (int)(cs % Y::kKSlots);
+          if (!wait(c, A_K_EMPTY + s, ((cs / Y::kKSlots) & 1u) ^ 1u)) return false;
+          uint8_t* kd = smem + Y::A_OffK + s * kKChunkBytes;
+          for (int q = gt; q < 512; q += kGT) {
+            const int r = q >> 2, rp = q & 3;
+            uint4 o0, o1;
+            dequant16(*(const uint4*)(raw + q * 16), sc[r * 4 + (k >> 1)], o0, o1);
+            *(uint4*)(kd + sw128_off((uint32_t)r, (uint32_t)(2 * rp))) = o0;
+            *(uint4*)(kd + sw128_off((uint32_t)r, (uint32_t)(2 * rp + 1))) = o1;
+          }
+          mbar_arrive(c.bar(A_K_FULL + s));
+        } else {  // FP4: unit k = latent chunks 2k and 2k + 1 (piece rp of a row = 32 channels)
+          const uint32_t cs0 = b * (uint32_t)kChunksPerBlock + 2u * (uint32_t)k;
+          const int s0 = (int)(cs0 % Y::kKSlots), s1 = (int)((cs0 + 1u) % Y::kKSlots);
+          if (!wait(c, A_K_EMPTY + s0, ((cs0 / Y::kKSlots) & 1u) ^ 1u) ||
+              !wait(c, A_K_EMPTY + s1, (((cs0 + 1u) / Y::kKSlots) & 1u) ^ 1u))
+            return false;
+          for (int q = gt; q < 512; q += kGT) {
+            const int r = q >> 2, rp = q & 3;
+            uint4 o[4];
+            dequant32_fp4(*(const uint4*)(raw + q * 16), sc[r * 16 + 4 * k + rp], o);
+            uint8_t* kd = smem + Y::A_OffK + (rp < 2 ? s0 : s1) * kKChunkBytes;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) *(uint4*)(kd + sw128_off((uint32_t)r, (uint32_t)(4 * (rp & 1) + j))) = o[j];
+          }
+          mbar_arrive(c.bar(A_K_FULL + s0));
+          mbar_arrive(c.bar(A_K_FULL + s1));
         }
-      } else {
+      } else {  // rope half: 32 bf16 of chunk 8, which completes with the second half
+        const int hr = k - R::kLatUnits;
+        const uint32_t cs = b * (uint32_t)kChunksPerBlock + 8u;
+        const int s = (int)(cs % Y::kKSlots);
+        if (hr == 0 && !wait(c, A_K_EMPTY + s, ((cs / Y::kKSlots) & 1u) ^ 1u)) return false;
+        uint8_t* kd = smem + Y::A_OffK + s * kKChunkBytes;
         for (int q = gt; q < 512; q += kGT)
-          *(uint4*)(kd + sw128_off((uint32_t)(q >> 2), (uint32_t)(4 * (k - 8) + (q & 3)))) = *(const uint4*)(raw + q * 16);
+          *(uint4*)(kd + sw128_off((uint32_t)(q >> 2), (uint32_t)(4 * hr + (q & 3)))) = *(const uint4*)(raw + q * 16);
+        if (hr == 1) mbar_arrive(c.bar(A_K_FULL + s));
       }
-      if (k != 8) mbar_arrive(c.bar(A_K_FULL + s));  // chunk 8 (rope) completes with unit 9
       __syncwarp();
       if (lane == 0) mbar_arrive(c.bar(RAW_EMPTY + rs));
-      if (k == 9 && lane == 0) mbar_arrive(c.bar(IDX_EMPTY + (int)(b % kIdxSlots)));
+      if (k == R::kUnits - 1 && lane == 0) mbar_arrive(c.bar(IDX_EMPTY + (int)(b % kIdxSlots)));
       return true;
     };
     for (uint32_t u = 0; u < 2u && u < nunits && ok; ++u) ok = issue(u);
@@ -464,7 +532,7 @@ static __device__ void qk_gather_fp8(const Ctx& c, const FwdParams& p) {
 // lanes cp.async the 128 rope bytes of the 8 rows straight into the group's swizzled rope atom.  The
 // group's landing barrier completes on the bulk bytes plus one cp.async arrival per lane.
 static __device__ void qk_issue_bf16(const Ctx& c, const FwdParams& p) {
-  using Y = Lay<false>;
+  using Y = Lay<kFmtBf16>;
   const int lane = c.lane, i = c.warp - 12;
   const int* lists = (const int*)(c.smem + Y::OffIdx);
   const uint32_t nblk = blocks_of_pair(p, c.pair);
@@ -510,7 +578,7 @@ static __device__ void qk_issue_bf16(const Ctx& c, const FwdParams& p) {
 // bf16 rows, transposers (warps 1 and 3): once a group has landed, turn its latent rows into SW128
 // atoms in place and count the group towards its half.
 static __device__ void qk_transpose_bf16(const Ctx& c, const FwdParams& p) {
-  using Y = Lay<false>;
+  using Y = Lay<kFmtBf16>;
   const int lane = c.lane, t = (c.warp == 1) ? 0 : 1;
   const uint32_t nblk = blocks_of_pair(p, c.pair);
   bool ok = true;
@@ -527,9 +595,10 @@ static __device__ void qk_transpose_bf16(const Ctx& c, const FwdParams& p) {
   if (!ok) set_abort(c);
 }
 
-template <bool kFp8>
+template <int kFmt>
 __device__ void qk_mma(const Ctx& c, const FwdParams& p) {
-  using Y = Lay<kFp8>;
+  using Y = Lay<kFmt>;
+  constexpr bool kQuant = kFmt != kFmtBf16;
   if (c.lane == 0) {
     PieceIter it;
     it.init(p.cum, p.s_q, c.pair, p.npairs);
@@ -545,7 +614,7 @@ __device__ void qk_mma(const Ctx& c, const FwdParams& p) {
         if (!wait(c, A_S_EMPTY + sb, ((blk >> 1) & 1u) ^ 1u)) { ok = false; break; }
         tc_fence_after();
         const uint32_t dS = c.tmem + kTmS + (uint32_t)sb * kBT;
-        if constexpr (!kFp8) {
+        if constexpr (!kQuant) {
           // bf16: each half of 64 rows as soon as its 8 groups are laid out (N = 64), then free it
           for (int h = 0; h < 2 && ok; ++h) {
             if (!wait(c, A_KH_FULL + h, blk & 1u)) { ok = false; break; }
@@ -599,9 +668,9 @@ __device__ void qk_mma(const Ctx& c, const FwdParams& p) {
   __syncwarp();
 }
 
-template <bool kFp8>
+template <int kFmt>
 __device__ void qk_softmax(const Ctx& c, const FwdParams& p) {
-  using Y = Lay<kFp8>;
+  using Y = Lay<kFmt>;
   uint8_t* smem = c.smem;
   const int warp = c.warp, lane = c.lane;
   const int sw = warp - 4;
@@ -745,8 +814,10 @@ __device__ void qk_softmax(const Ctx& c, const FwdParams& p) {
 
 // ============================================================================ PV side
 // FP8 rows: cp.async into a raw ring, dequantised by the same warps into the V row-group ring.
-static __device__ void pv_gather_fp8(const Ctx& c, const FwdParams& p) {
-  using Y = Lay<true>;
+template <int kFmt>
+static __device__ void pv_gather_q(const Ctx& c, const FwdParams& p) {
+  using Y = Lay<kFmt>;
+  using R = QRow<kFmt>;
   uint8_t* smem = c.smem;
   const int warp = c.warp, lane = c.lane;
   const int gw = (warp == 1) ? 0 : warp - 7;  // 0..8
@@ -756,8 +827,8 @@ static __device__ void pv_gather_fp8(const Ctx& c, const FwdParams& p) {
   const uint32_t nblk = blocks_of_pair(p, c.pair);
   bool ok = true;
   {
-    // Per 16-row group one raw unit: the first 528 bytes of each row (512 e4m3 + 4 fp32 scales),
-    // staged two units ahead, then dequantised into the MN-major V row-group ring.
+    // Per 16-row group one raw unit: the codes and scales at the start of each row (528 bytes for FP8,
+    // 320 for FP4), staged two units ahead, then dequantised into the MN-major V row-group ring.
     const uint32_t nunits = nblk * (uint32_t)kGroupsPerBlock;
     auto issue = [&](uint32_t u) -> bool {
       const uint32_t b = u / (uint32_t)kGroupsPerBlock;
@@ -765,10 +836,11 @@ static __device__ void pv_gather_fp8(const Ctx& c, const FwdParams& p) {
       if (!wait(c, RAW_EMPTY + rs, ((u / kRawSlots) & 1u) ^ 1u)) return false;
       if (g == 0 && !wait(c, IDX_FULL + (int)(b % kIdxSlots), (b / kIdxSlots) & 1u)) return false;
       const int* l = lists + (int)(b % kIdxSlots) * kIdxSlotInts + g * kVGroupRows;
-      const uint32_t dst = c.sbase + Y::B_OffRaw + (uint32_t)rs * kRawBSlot;
-      for (int q = gt; q < kVGroupRows * 33; q += kGT) {
-        const int rr = q / 33, pc = q - rr * 33;
-        cp_async16(dst + (uint32_t)q * 16u, p.kv + (size_t)l[rr] * kFp8RowBytes + 16 * pc);
+      const uint32_t dst = c.sbase + Y::B_OffRaw + (uint32_t)rs * R::kRawBSlot;
+      constexpr int kPer = R::kRawBRow / 16;  // 16-byte pieces per row
+      for (int q = gt; q < kVGroupRows * kPer; q += kGT) {
+        const int rr = q / kPer, pc = q - rr * kPer;
+        cp_async16(dst + (uint32_t)q * 16u, p.kv + (size_t)l[rr] * R::kBytes + 16 * pc);
       }
       cp_async_arrive(c.bar(RAW_FULL + rs));
       return true;
@@ -779,16 +851,28 @@ static __device__ void pv_gather_fp8(const Ctx& c, const FwdParams& p) {
       if (!wait(c, RAW_FULL + rs, (u / kRawSlots) & 1u)) return false;
       const int s = (int)(u % Y::kVSlots);
       if (!wait(c, B_V_EMPTY + s, ((u / Y::kVSlots) & 1u) ^ 1u)) return false;
-      const uint8_t* raw = smem + Y::B_OffRaw + rs * kRawBSlot;
+      const uint8_t* raw = smem + Y::B_OffRaw + rs * R::kRawBSlot;
       uint8_t* vd = smem + Y::B_OffV + s * kVGroupBytes;
-      for (int q = gt; q < kVGroupRows * 32; q += kGT) {
-        const int rr = q >> 5, pc = q & 31;
-        const uint8_t* rrow = raw + rr * kRawBRowBytes;
-        uint4 o0, o1;
-        dequant16(*(const uint4*)(rrow + pc * 16), *(const float*)(rrow + 512 + 4 * (pc >> 3)), o0, o1);
-        uint8_t* chunk = vd + (pc >> 2) * 2048;
-        *(uint4*)(chunk + sw128_off((uint32_t)rr, (uint32_t)(2 * (pc & 3)))) = o0;
-        *(uint4*)(chunk + sw128_off((uint32_t)rr, (uint32_t)(2 * (pc & 3) + 1))) = o1;
+      if constexpr (!R::kF4) {  // FP8: piece pc of a row = 16 channels; scale per 128 channels
+        for (int q = gt; q < kVGroupRows * 32; q += kGT) {
+          const int rr = q >> 5, pc = q & 31;
+          const uint8_t* rrow = raw + rr * R::kRawBRow;
+          uint4 o0, o1;
+          dequant16(*(const uint4*)(rrow + pc * 16), *(const float*)(rrow + R::kScaleOff + 4 * (pc >> 3)), o0, o1);
+          uint8_t* chunk = vd + (pc >> 2) * 2048;
+          *(uint4*)(chunk + sw128_off((uint32_t)rr, (uint32_t)(2 * (pc & 3)))) = o0;
+          *(uint4*)(chunk + sw128_off((uint32_t)rr, (uint32_t)(2 * (pc & 3) + 1))) = o1;
+        }
+      } else {  // FP4: piece pc of a row = 32 channels = its own scale group
+        for (int q = gt; q < kVGroupRows * 16; q += kGT) {
+          const int rr = q >> 4, pc = q & 15;
+          const uint8_t* rrow = raw + rr * R::kRawBRow;
+          uint4 o[4];
+          dequant32_fp4(*(const uint4*)(rrow + pc * 16), *(const float*)(rrow + R::kScaleOff + 4 * pc), o);
+          uint8_t* chunk = vd + (pc >> 1) * 2048;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) *(uint4*)(chunk + sw128_off((uint32_t)rr, (uint32_t)(4 * (pc & 1) + j))) = o[j];
+        }
       }
       mbar_arrive(c.bar(B_V_FULL + s));
       __syncwarp();
@@ -808,7 +892,7 @@ static __device__ void pv_gather_fp8(const Ctx& c, const FwdParams& p) {
 // bf16 rows, issuers (warps 8..13): slot group g of block b holds rows 16g..16g+15 as two 8-row units;
 // lane j < 16 bulk-copies the 1024 latent bytes (= V) of row 16g + j into unit j / 8 as a plain row.
 static __device__ void pv_issue_bf16(const Ctx& c, const FwdParams& p) {
-  using Y = Lay<false>;
+  using Y = Lay<kFmtBf16>;
   const int lane = c.lane, i = c.warp - 8;
   const int* lists = (const int*)(c.smem + Y::OffIdx);
   const uint32_t nblk = blocks_of_pair(p, c.pair);
@@ -847,7 +931,7 @@ static __device__ void pv_issue_bf16(const Ctx& c, const FwdParams& p) {
 
 // bf16 rows, transposers (warps 1, 14, 15): lay out both units of a landed slot group and hand it to the MMA.
 static __device__ void pv_transpose_bf16(const Ctx& c, const FwdParams& p) {
-  using Y = Lay<false>;
+  using Y = Lay<kFmtBf16>;
   const int lane = c.lane, t = (c.warp == 1) ? 0 : c.warp - 13;
   const uint32_t total = blocks_of_pair(p, c.pair) * (uint32_t)kGroupsPerBlock;
   bool ok = true;
@@ -864,9 +948,10 @@ static __device__ void pv_transpose_bf16(const Ctx& c, const FwdParams& p) {
   if (!ok) set_abort(c);
 }
 
-template <bool kFp8>
+template <int kFmt>
 __device__ void pv_mma(const Ctx& c, const FwdParams& p) {
-  using Y = Lay<kFp8>;
+  using Y = Lay<kFmt>;
+  constexpr bool kQuant = kFmt != kFmtBf16;
   if (c.lane == 0) {
     PieceIter it;
     it.init(p.cum, p.s_q, c.pair, p.npairs);
@@ -895,7 +980,7 @@ __device__ void pv_mma(const Ctx& c, const FwdParams& p) {
           // V of 16 rows, MN-major: 64-column chunks LBO apart, the two 8-row atoms along K SBO apart.
           // bf16 groups are two transposed units (chunk stride 1 KB, unit stride 8 KB); FP8 groups are
           // dequantised chunk-major (chunk stride 2 KB, atom stride 1 KB).
-          constexpr uint32_t kLbo = kFp8 ? 2048u : 1024u, kSbo = kFp8 ? 1024u : (uint32_t)kUnitBytes;
+          constexpr uint32_t kLbo = kQuant ? 2048u : 1024u, kSbo = kQuant ? 1024u : (uint32_t)kUnitBytes;
           mma_ss(c.tmem + 0, adesc, smem_desc(vs, kLbo, kSbo), kIdescPV, acc);
           mma_ss(c.tmem + 256, adesc, smem_desc(vs + 4u * kLbo, kLbo, kSbo), kIdescPV, acc);
           mma_commit(c.bar(B_V_EMPTY + s));
@@ -934,9 +1019,9 @@ __device__ __forceinline__ void pv_slot_return(const Ctx& c, const FwdParams& p)
   __syncwarp();
 }
 
-template <bool kFp8>
+template <int kFmt>
 __device__ void pv_epilogue(const Ctx& c, const FwdParams& p) {
-  using Y = Lay<kFp8>;
+  using Y = Lay<kFmt>;
   uint8_t* smem = c.smem;
   const int lane = c.lane;
   const int quarter = c.warp & 3;
@@ -1024,10 +1109,11 @@ __device__ void pv_epilogue(const Ctx& c, const FwdParams& p) {
 
 }  // namespace fwd
 
-template <bool kFp8>
+template <int kFmt>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(fwd::kThreads, 1) dsa_fwd_kernel(const FwdParams p) {
   using namespace fwd;
-  using Y = Lay<kFp8>;
+  using Y = Lay<kFmt>;
+  constexpr bool kQuant = kFmt != kFmtBf16;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   Ctx c;
   c.smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -1045,7 +1131,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(fwd::kThreads, 1) ds
 
   if (threadIdx.x == 0) {
     const int gwarps = (c.rank == 0) ? kGatherWarpsA : kGatherWarpsB;
-    const int list_users = kFp8 ? gwarps : (c.rank == 0 ? kIssuersA : kIssuersB);
+    const int list_users = kQuant ? gwarps : (c.rank == 0 ? kIssuersA : kIssuersB);
     for (int q = 0; q < kIdxSlots; ++q) {
       mbar_init(c.bar(IDX_FULL + q), 1);
       mbar_init(c.bar(IDX_EMPTY + q), list_users);
@@ -1055,7 +1141,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(fwd::kThreads, 1) ds
       mbar_init(c.bar(RAW_EMPTY + q), gwarps);
     }
     if (c.rank == 0) {
-      if constexpr (kFp8) {
+      if constexpr (kQuant) {
         for (int s = 0; s < Y::kKSlots; ++s) {
           mbar_init(c.bar(A_K_FULL + s), kGatherWarpsA * 32);
           mbar_init(c.bar(A_K_EMPTY + s), 1);
@@ -1079,7 +1165,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(fwd::kThreads, 1) ds
       mbar_init(c.bar(A_DRAIN), 1);
     } else {
       for (int s = 0; s < Y::kVSlots; ++s) {
-        mbar_init(c.bar(B_V_FULL + s), kFp8 ? kGatherWarpsB * 32 : 1);
+        mbar_init(c.bar(B_V_FULL + s), kQuant ? kGatherWarpsB * 32 : 1);
         mbar_init(c.bar(B_V_EMPTY + s), 1);
         mbar_init(c.bar(B_V_LAND + s), 1 + 32);  // expect_tx + cp.async
       }
@@ -1107,29 +1193,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(fwd::kThreads, 1) ds
 
   const int w = c.warp;
   if (w == 0) {
-    index_compactor<kFp8>(c, p);
+    index_compactor<kFmt>(c, p);
   } else if (w == 2) {
-    if (c.rank == 0) qk_mma<kFp8>(c, p);
-    else pv_mma<kFp8>(c, p);
+    if (c.rank == 0) qk_mma<kFmt>(c, p);
+    else pv_mma<kFmt>(c, p);
   } else if (c.rank == 0) {
-    if constexpr (kFp8) {
-      if (w == 1 || w >= 12) qk_gather_fp8(c, p);
-      else if (w >= 4) qk_softmax<kFp8>(c, p);
+    if constexpr (kQuant) {
+      if (w == 1 || w >= 12) qk_gather_q<kFmt>(c, p);
+      else if (w >= 4) qk_softmax<kFmt>(c, p);
     } else {
       if (w >= 12) qk_issue_bf16(c, p);
-      else if (w >= 4) qk_softmax<kFp8>(c, p);
+      else if (w >= 4) qk_softmax<kFmt>(c, p);
       else qk_transpose_bf16(c, p);  // warps 1, 3
     }
   } else {
-    if constexpr (kFp8) {
-      if (w == 1 || w >= 8) pv_gather_fp8(c, p);
+    if constexpr (kQuant) {
+      if (w == 1 || w >= 8) pv_gather_q<kFmt>(c, p);
       else if (w == 3) pv_slot_return(c, p);
-      else if (w >= 4) pv_epilogue<kFp8>(c, p);
+      else if (w >= 4) pv_epilogue<kFmt>(c, p);
     } else {
       if (w >= 8 && w < 14) pv_issue_bf16(c, p);
       else if (w == 1 || w >= 14) pv_transpose_bf16(c, p);
       else if (w == 3) pv_slot_return(c, p);
-      else if (w >= 4) pv_epilogue<kFp8>(c, p);
+      else if (w >= 4) pv_epilogue<kFmt>(c, p);
     }
   }
 
@@ -1141,15 +1227,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(fwd::kThreads, 1) ds
 }
 
 // Largest number of 2-CTA clusters of the kernel that fit at once on the current device.
-template <bool kFp8>
+template <int kFmt>
 int max_active_pairs_impl() {
   static int cached = -1;
   static int cached_dev = -1;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
   if (cached >= 0 && cached_dev == dev) return cached;
-  constexpr int smem = fwd::Lay<kFp8>::SmemAlloc;
-  if (cudaFuncSetAttribute(dsa_fwd_kernel<kFp8>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+  constexpr int smem = fwd::Lay<kFmt>::SmemAlloc;
+  if (cudaFuncSetAttribute(dsa_fwd_kernel<kFmt>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
     return 0;
   int sms = 0;
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -1158,7 +1244,7 @@ int max_active_pairs_impl() {
   cfg.blockDim = dim3(fwd::kThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   int nclusters = 0;
-  if (cudaOccupancyMaxActiveClusters(&nclusters, dsa_fwd_kernel<kFp8>, &cfg) != cudaSuccess || nclusters <= 0) {
+  if (cudaOccupancyMaxActiveClusters(&nclusters, dsa_fwd_kernel<kFmt>, &cfg) != cudaSuccess || nclusters <= 0) {
     cudaGetLastError();
     return 0;
   }
@@ -1167,12 +1253,12 @@ int max_active_pairs_impl() {
   return cached;
 }
 
-template <bool kFp8>
+template <int kFmt>
 cudaError_t launch_impl(const FwdParams& p, cudaStream_t stream) {
-  constexpr int smem = fwd::Lay<kFp8>::SmemAlloc;
-  cudaError_t e = cudaFuncSetAttribute(dsa_fwd_kernel<kFp8>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  constexpr int smem = fwd::Lay<kFmt>::SmemAlloc;
+  cudaError_t e = cudaFuncSetAttribute(dsa_fwd_kernel<kFmt>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  dsa_fwd_kernel<kFp8><<<2 * p.npairs, fwd::kThreads, smem, stream>>>(p);
+  dsa_fwd_kernel<kFmt><<<2 * p.npairs, fwd::kThreads, smem, stream>>>(p);
   return cudaGetLastError();
 }
 

@@ -127,8 +127,10 @@ def quantize_fp4_rows(latent: np.ndarray, rope_bf16: torch.Tensor) -> torch.Tens
     amax = np.abs(g).max(axis=2)
     scale = np.where(amax > 0, amax / np.float32(6.0), np.float32(1.0)).astype(np.float32)
     y = np.abs(g) / scale[:, :, None]
-    d = np.abs(y[..., None] - _E2M1_GRID) + (np.arange(8) & 1) * np.float32(1e-6)  # ties -> even code
-    mag = d.argmin(axis=-1).astype(np.uint8)
+    mids = (_E2M1_GRID[1:] + _E2M1_GRID[:-1]) / 2  # y between mids[i-1] and mids[i] -> code i
+    lo = np.searchsorted(mids, y, side="left")
+    hi = np.searchsorted(mids, y, side="right")
+    mag = np.where((lo != hi) & (lo % 2 == 1), hi, lo).astype(np.uint8)  # a tie goes to the even code
     codes = (mag | np.where(g < 0, 8, 0).astype(np.uint8)).reshape(n, D_V)
     rows = np.empty((n, FP4_ROW_BYTES), dtype=np.uint8)
     rows[:, :D_V // 2] = codes[:, 0::2] | (codes[:, 1::2] << 4)

@@ -1,9 +1,9 @@
 """Helpers for GPU-vs-oracle parity tests (tolerances written here, used by every test).
 
 Tolerances: lse within 2e-3 absolute; out max-abs error <= 1e-2 * max|out_ref| + 1e-3
-for a bf16 KV cache and <= 3e-2 * max|out_ref| for an FP8 cache (the oracle is fed
-the dequantised rows, so the FP8 bound covers the bf16 rounding of the dequantised
-values before the tensor cores).
+for a bf16 KV cache and <= 3e-2 * max|out_ref| for an FP8 or FP4 cache (the oracle is
+fed the dequantised rows, so the quantised-cache bound covers the bf16 rounding of P
+and of the dequantised values before the tensor cores).
 """
 import numpy as np
 import torch
@@ -20,7 +20,7 @@ def bits(t: torch.Tensor) -> np.ndarray:
 
 
 def kv_raw(wl) -> np.ndarray:
-    return wl.kv.numpy() if wl.kv_format == "fp8" else bits(wl.kv)
+    return bits(wl.kv) if wl.kv_format == "bf16" else wl.kv.numpy()
 
 
 def oracle(wl, tokens=None):
@@ -39,7 +39,7 @@ def oracle_paged(wl, tokens=None):
 
 def run_gpu_paged(wl, device="cuda"):
     from sparse_mla_attention_dsa_gb300 import api
-    fmt = api.KV_BF16 if wl.kv_format == "bf16" else api.KV_FP8
+    fmt = {"bf16": api.KV_BF16, "fp8": api.KV_FP8, "fp4": api.KV_FP4}[wl.kv_format]
     out, lse = api.dsa_sparse_attn_fwd_paged(wl.q.to(device), wl.kv.to(device), wl.indices.to(device),
                                              wl.meta["seq_of_token"].to(device), wl.meta["block_table"].to(device),
                                              wl.meta["page_size"], wl.sm_scale, kv_format=fmt, check_status=True)
@@ -52,7 +52,8 @@ def run_gpu(wl, device="cuda"):
     q = wl.q.to(device)
     kv = wl.kv.to(device)
     idx = wl.indices.to(device)
-    fn = api.dsa_sparse_attn_fwd if wl.kv_format == "bf16" else api.dsa_sparse_attn_fwd_fp8kv
+    fn = {"bf16": api.dsa_sparse_attn_fwd, "fp8": api.dsa_sparse_attn_fwd_fp8kv,
+          "fp4": api.dsa_sparse_attn_fwd_fp4kv}[wl.kv_format]
     out, lse = fn(q, kv, idx, wl.sm_scale, check_status=True)
     torch.cuda.synchronize()
     return out, lse

@@ -169,3 +169,27 @@ def test_decode_fp8_full_size_sampled():
     wl = W.decode_fp8()
     out, lse = P.run_gpu(wl)
     _check(wl, tokens=[0, 1, 50, 99, 127], out=out, lse=lse)
+
+
+# ---------------------------------------------------------------- FP4 (e2m1) KV cache
+
+@pytest.mark.parametrize("s_q,h_q,s_kv,topk,bad", [
+    (4, 128, 600, 300, 0.0),
+    (9, 64, 2000, 257, 0.1),
+    (3, 16, 300, 129, 0.0),
+])
+def test_fp4_small_shapes(s_q, h_q, s_kv, topk, bad):
+    _check(W.small_random(51 + s_q, s_q, h_q, s_kv, topk, kv_format="fp4", invalid_frac=bad, q_sigma=2.0))
+
+
+def test_fp4_masked_tokens_and_split_work():
+    wl = W.small_random(55, 200, 128, 4096, 512, kv_format="fp4", invalid_frac=0.05, q_sigma=2.0)
+    wl.indices[3] = -1  # a token with no valid slot
+    _check(wl, tokens=list(range(0, 200, 9)) + [3])
+
+
+@pytest.mark.slow
+def test_decode_fp4_full_size_sampled():
+    wl = W.decode_fp4()
+    out, lse = P.run_gpu(wl)
+    _check(wl, tokens=[0, 1, 50, 99, 127], out=out, lse=lse)
