@@ -24,8 +24,9 @@ def _declared_symbols():
 
 def test_header_declares_the_entry_points():
     names = _declared_symbols()
-    assert {"dsa_sparse_attn_fwd", "dsa_sparse_attn_fwd_fp8kv", "dsa_sparse_attn_fwd_workspace_size",
-            "dsa_read_device_status", "dsa_status_string", "dsa_kernels_per_call"} <= set(names)
+    assert {"dsa_sparse_attn_fwd", "dsa_sparse_attn_fwd_fp8kv", "dsa_sparse_attn_fwd_fp4kv",
+            "dsa_sparse_attn_fwd_paged", "dsa_sparse_attn_fwd_workspace_size", "dsa_read_device_status",
+            "dsa_status_string", "dsa_kernels_per_call"} <= set(names)
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -58,3 +59,26 @@ def test_host_validation_needs_no_device(lib):
     assert f(bad, bad, bad, 2, 16, 10, 4, ctypes.c_float(0.1), bad, bad, bad, ctypes.c_size_t(0), null) == 3
     assert lib.dsa_sparse_attn_fwd_workspace_size(-1, 16, 4, 0) == 0
     assert lib.dsa_sparse_attn_fwd_workspace_size(4, 16, 4, 7) == 0
+
+
+def test_fp4_and_paged_host_validation_needs_no_device(lib):
+    null = ctypes.c_void_p(0)
+    f4 = lib.dsa_sparse_attn_fwd_fp4kv
+    assert f4(null, null, null, 0, 16, 10, 4, ctypes.c_float(0.1), null, null, null, ctypes.c_size_t(0), null) == 0
+    assert f4(null, null, null, 2, 129, 10, 4, ctypes.c_float(0.1), null, null, null, ctypes.c_size_t(0), null) == 1
+    assert f4(null, null, null, 2, 16, 10, 4, ctypes.c_float(0.1), null, null, null, ctypes.c_size_t(0), null) == 1
+
+    pg = lib.dsa_sparse_attn_fwd_paged
+    ok_ptr = ctypes.c_void_p(0x1000)
+
+    def call(fmt=0, seq=ok_ptr, table=ok_ptr, s_q=2, n_seq=1, max_pages=4, page=16):
+        return pg(fmt, null, null, null, seq, table, s_q, 16, 64, 4, n_seq, max_pages, page, ctypes.c_float(0.1),
+                  null, null, null, ctypes.c_size_t(0), null)
+
+    assert call(fmt=3) == 1                                   # unknown KV format
+    assert call(n_seq=0) == 1 and call(max_pages=0) == 1 and call(page=0) == 1
+    assert call(n_seq=1 << 20, max_pages=1 << 12) == 1        # table of 2^32 entries
+    assert call(seq=null) == 1 and call(table=null) == 1      # tables needed when there are tokens
+    assert call(seq=ctypes.c_void_p(0x1002)) == 3             # int32 tables need 4-byte alignment
+    assert call(s_q=0, seq=null, table=null) == 0             # nothing to do
+    assert call() == 1                                        # passes the table checks, then null data pointers
