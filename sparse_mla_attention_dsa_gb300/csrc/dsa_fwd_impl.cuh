@@ -229,29 +229,33 @@ __device__ __forceinline__ uint32_t sw128_off(uint32_t row, uint32_t chunk16) {
   return (row >> 3) * 1024 + (row & 7) * 128 + ((chunk16 ^ (row & 7)) << 4);
 }
 
-// In-place re-layout of one 8-row unit: 8 rows of 512 bf16 landed as plain rows (row r at r*1024) become
-// 8 SW128 atoms (64-column chunk c at c*1024, row r at r*128 inside it, 16-byte pieces XOR-swizzled by r).
-// As 128-byte segments this is an 8x8 transpose; the segments with (r + c) even and with (r + c) odd are
-// each closed under it, so a warp moves each class through registers (8 pieces per lane) in one step.
-__device__ __forceinline__ void transpose_unit(uint8_t* un, int lane) {
+// In-place re-layout of one 8-row unit at shared address `un`: 8 rows of 512 bf16 landed as plain rows
+// (row r at r*1024) become 8 SW128 atoms (64-column chunk c at c*1024, row r at r*128 inside it, 16-byte
+// pieces XOR-swizzled by r).  As 128-byte segments this is an 8x8 transpose; the segments with (r + c)
+// even and with (r + c) odd are each closed under it and disjoint, so a warp moves one class through
+// registers (8 pieces per lane), then the other, with one sync between the reads and the writes of each.
+// A warp instruction touches 4 whole 128-byte segments, so neither side has bank conflicts.
+__device__ __forceinline__ uint4 lds128(uint32_t a) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ void sts128(uint32_t a, uint4 v) {
+  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
+}
+__device__ __forceinline__ void transpose_unit(uint32_t un, int lane) {
+  const int k = lane & 7, cb = 2 * (lane >> 3);
 #pragma unroll
   for (int ph = 0; ph < 2; ++ph) {
     uint4 v[8];
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      const int sidx = q * 4 + (lane >> 3), k = lane & 7;
-      const int r = sidx >> 2, c = 2 * (sidx & 3) + ((r + ph) & 1);
-      v[q] = *(const uint4*)(un + r * 1024 + c * 128 + k * 16);
-    }
+    for (int r = 0; r < 8; ++r) v[r] = lds128(un + (uint32_t)(r * 1024 + (cb + ((r + ph) & 1)) * 128 + k * 16));
     __syncwarp();
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      const int sidx = q * 4 + (lane >> 3), k = lane & 7;
-      const int r = sidx >> 2, c = 2 * (sidx & 3) + ((r + ph) & 1);
-      *(uint4*)(un + c * 1024 + sw128_off((uint32_t)r, (uint32_t)k)) = v[q];
-    }
-    __syncwarp();
+    for (int r = 0; r < 8; ++r)
+      sts128(un + (uint32_t)((cb + ((r + ph) & 1)) * 1024) + sw128_off((uint32_t)r, (uint32_t)k), v[r]);
   }
+  __syncwarp();
 }
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
@@ -586,7 +590,7 @@ static __device__ void qk_transpose_bf16(const Ctx& c, const FwdParams& p) {
     for (int g = t; g < 2 * kGroupsPerHalf; g += kTransA) {
       const int h = g / kGroupsPerHalf, gg = g % kGroupsPerHalf;
       if (!wait(c, A_LAND + g, b & 1u)) { ok = false; break; }
-      if (gg < kBulkGroupsA) transpose_unit(c.smem + Y::A_OffK + h * kHalfLatBytes + gg * kUnitBytes, lane);
+      if (gg < kBulkGroupsA) transpose_unit(c.sbase + Y::A_OffK + (uint32_t)(h * kHalfLatBytes + gg * kUnitBytes), lane);
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(c.bar(A_KH_FULL + h));
@@ -938,9 +942,9 @@ static __device__ void pv_transpose_bf16(const Ctx& c, const FwdParams& p) {
   for (uint32_t gs = (uint32_t)t; gs < total; gs += kTransB) {
     const int s = (int)(gs % Y::kVSlots);
     if (!wait(c, B_V_LAND + s, (gs / Y::kVSlots) & 1u)) { ok = false; break; }
-    uint8_t* grp = c.smem + Y::B_OffV + s * kVGroupBytes;
+    const uint32_t grp = c.sbase + Y::B_OffV + (uint32_t)(s * kVGroupBytes);
     transpose_unit(grp, lane);
-    if ((int)(gs % (uint32_t)kGroupsPerBlock) < kBulkUnit1B) transpose_unit(grp + kUnitBytes, lane);
+    if ((int)(gs % (uint32_t)kGroupsPerBlock) < kBulkUnit1B) transpose_unit(grp + (uint32_t)kUnitBytes, lane);
     fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) mbar_arrive(c.bar(B_V_FULL + s));
