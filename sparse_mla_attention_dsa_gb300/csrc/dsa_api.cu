@@ -40,9 +40,18 @@ __global__ void __launch_bounds__(kPrepWarps * 32) dsa_prep_kernel(const FwdPara
   const int t = blockIdx.x * kPrepWarps + warp;
   if (t < s_q) {
     const int32_t* row = p.indices + (size_t)t * topk;
-    const int seq = token_seq(p, t);
     int c = 0;
-    for (int i = lane; i < topk; i += 32) c += resolve_row(p, seq, __ldg(row + i)) >= 0 ? 1 : 0;
+    if (p.pg.block_table == nullptr) {  // flat layout: a row id is valid inside [0, s_kv)
+      const int s_kv = p.s_kv;
+#pragma unroll 4
+      for (int i = lane; i < topk; i += 32) {
+        const int v = __ldg(row + i);
+        c += (v >= 0 && v < s_kv) ? 1 : 0;
+      }
+    } else {
+      const int seq = token_seq(p, t);
+      for (int i = lane; i < topk; i += 32) c += resolve_row(p, seq, __ldg(row + i)) >= 0 ? 1 : 0;
+    }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
     if (lane == 0) nvalid[t] = c;
