@@ -8,8 +8,9 @@ the whole batch (counting/scheduling kernel, attention kernel, split-token merge
 
 Prints ONE JSON line (rank 0).  FLOPs per token = 2 * h_q * n_valid * (576 + 512);
 ``value`` is whole-job TFLOP/s with inputs resident in HBM; ``e2e`` is the same
-metric through the public API with pinned host buffers (H2D of the inputs and
-D2H of out/lse inside every timed step); ``roofline`` is the attention kernel
+metric through the public host-buffer entry point dsa_sparse_attn_fwd_host
+(pinned host buffers; H2D of the inputs and D2H of out/lse inside every timed
+step, pipelined by token chunks of ``--e2e-chunk``); ``roofline`` is the attention kernel
 alone (CUDA events recorded around it inside the library call) against the
 bound that dominates max(FLOPs / bf16 peak, algorithmic bytes / HBM peak), the
 algorithmic bytes being the gathered KV rows plus Q, out, lse and indices;
@@ -273,13 +274,24 @@ def _e2e(args, wl, q, kv, idx, out, lse, step, stream, world, dev):
     outh = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     lseh = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
 
-    def e2e_step():
-        q.copy_(qh, non_blocking=True)
-        kv.copy_(kvh, non_blocking=True)
-        idx.copy_(idxh, non_blocking=True)
-        step()
-        outh.copy_(out, non_blocking=True)
-        lseh.copy_(lse, non_blocking=True)
+    if wl.meta.get("paged"):
+        def e2e_step():  # the paged entry point takes device buffers: copies around it on one stream
+            q.copy_(qh, non_blocking=True)
+            kv.copy_(kvh, non_blocking=True)
+            idx.copy_(idxh, non_blocking=True)
+            step()
+            outh.copy_(out, non_blocking=True)
+            lseh.copy_(lse, non_blocking=True)
+    else:
+        from sparse_mla_attention_dsa_gb300 import api
+        fmt = {"bf16": api.KV_BF16, "fp8": api.KV_FP8, "fp4": api.KV_FP4}[wl.kv_format]
+        chunk = min(args.e2e_chunk, wl.s_q)
+        buf = torch.empty(api.dsa_sparse_attn_fwd_host_device_bytes(fmt, wl.s_q, wl.h_q, wl.s_kv, wl.topk, chunk),
+                          dtype=torch.uint8, device=dev)
+
+        def e2e_step():  # host buffers in and out; the call pipelines token chunks and returns when done
+            api.dsa_sparse_attn_fwd_host(qh, kvh, idxh, wl.sm_scale, kv_format=fmt, out=outh, lse=lseh,
+                                         device_buffer=buf, chunk_tokens=chunk, stream=stream)
 
     for _ in range(max(2, args.warmup)):
         e2e_step()
@@ -335,7 +347,11 @@ def _report(args, wl, flops, ms, kms, e2e_ms, clocks, world):
             "roofline": roof,
             "e2e": None if args.skip_e2e else {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
                                                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                                               "ms_per_step": e2e_ms},
+                                               "ms_per_step": e2e_ms,
+                                               "api": "dsa_sparse_attn_fwd_paged + torch copies"
+                                               if wl.meta.get("paged") else "dsa_sparse_attn_fwd_host",
+                                               "chunk_tokens": None if wl.meta.get("paged")
+                                               else min(args.e2e_chunk, wl.s_q)},
             "gpu_launches": K * api.dsa_kernels_per_call(),
             "clocks": clocks}
     if not args.no_cpu_baseline:
@@ -357,6 +373,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--s-q", type=int, default=4096, help="query tokens (4096 = the benchmark workload)")
     ap.add_argument("--skip-e2e", action="store_true")
+    ap.add_argument("--e2e-chunk", type=int, default=256,
+                    help="query tokens per chunk of the host-buffer pipeline timed as e2e")
     ap.add_argument("--workload", default="prefill_causal",
                     choices=["prefill_causal", "decode_bf16", "decode_fp8", "long_prefill", "decode_paged",
                              "decode_fp4", "tiny"])

@@ -169,6 +169,35 @@ DSA_API dsa_status dsa_sparse_attn_fwd_fp4kv(const void* q, const void* kv_fp4, 
                                              int s_kv, int topk, float sm_scale, void* out, float* lse,
                                              void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
+/* The forward from HOST buffers, the query tokens pipelined through the GPU in
+ * chunks of chunk_tokens.  The upload of a chunk's inputs, the forward of the
+ * chunk before it and the download of the chunk before that run at once, on
+ * two copy streams the call creates beside `stream`.  This is a convenience of
+ * this library: the method itself works on device memory only.
+ *   kv_format      DSA_KV_BF16, DSA_KV_FP8 or DSA_KV_FP4 (picks the row size of kv_host).
+ *   q_host, kv_host, indices_host, out_host, lse_host
+ *                  host memory with the layouts of dsa_sparse_attn_fwd (kv rows of
+ *                  1152, 656 or 448 bytes).  Page-locked memory (cudaHostAlloc)
+ *                  lets the copies overlap the compute; pageable memory works
+ *                  but serialises them.
+ *   device_buffer  >= dsa_sparse_attn_fwd_host_device_bytes(kv_format, s_q, h_q,
+ *                  s_kv, topk, chunk_tokens) bytes of device memory, 16-byte
+ *                  aligned, owned by the caller; it holds the whole KV, two sets of
+ *                  chunk buffers and a workspace, and its contents are scratch.
+ *   chunk_tokens   tokens per chunk, >= 1 (s_q or more: one chunk, no overlap).
+ * The work is queued after what `stream` already holds and the call returns
+ * when out_host and lse_host hold the result (it synchronises).  Returns
+ * DSA_ERR_INVALID_ARG / DSA_ERR_WORKSPACE / DSA_ERR_UNSUPPORTED before any
+ * copy for bad arguments, any error of the per-chunk forward, DSA_ERR_CUDA
+ * if a copy or synchronisation failed, or DSA_ERR_DEVICE_TIMEOUT if a bounded
+ * wait inside any chunk's kernels gave up (the outputs are then not valid). */
+DSA_API size_t dsa_sparse_attn_fwd_host_device_bytes(int kv_format, int s_q, int h_q, int s_kv, int topk,
+                                                     int chunk_tokens);
+DSA_API dsa_status dsa_sparse_attn_fwd_host(int kv_format, const void* q_host, const void* kv_host,
+                                            const int32_t* indices_host, int s_q, int h_q, int s_kv, int topk,
+                                            float sm_scale, void* out_host, float* lse_host, void* device_buffer,
+                                            size_t device_bytes, int chunk_tokens, cudaStream_t stream);
+
 /* Synchronises `stream` and returns the device-side status a previous forward
  * call left in `workspace` (DSA_OK or DSA_ERR_DEVICE_TIMEOUT), or DSA_ERR_CUDA
  * if the synchronisation itself failed. */

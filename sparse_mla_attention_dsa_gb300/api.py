@@ -38,6 +38,10 @@ def dsa_sparse_attn_fwd_workspace_size(s_q: int, h_q: int, topk: int, kv_format:
 def _check(q, kv, indices, kv_format):
     if not (q.is_cuda and kv.is_cuda and indices.is_cuda):
         raise ValueError("q, kv and indices must be CUDA tensors")
+    _check_shapes(q, kv, indices, kv_format)
+
+
+def _check_shapes(q, kv, indices, kv_format):
     if q.dtype != torch.bfloat16 or q.dim() != 3 or q.shape[2] != D_QK or not q.is_contiguous():
         raise ValueError("q must be a contiguous bf16 tensor [s_q, h_q, 576]")
     if kv_format == KV_BF16:
@@ -171,4 +175,43 @@ def dsa_sparse_attn_fwd_noalloc(q, kv, indices, sm_scale, out, lse, stream=None)
                                                  _stream_handle(stream))
     if st != 0:
         raise _lib.DsaError(st, "dsa_sparse_attn_fwd_noalloc")
+    return out, lse
+
+
+def dsa_sparse_attn_fwd_host_device_bytes(kv_format: int, s_q: int, h_q: int, s_kv: int, topk: int,
+                                          chunk_tokens: int) -> int:
+    return int(_lib.load().dsa_sparse_attn_fwd_host_device_bytes(kv_format, s_q, h_q, s_kv, topk, chunk_tokens))
+
+
+def dsa_sparse_attn_fwd_host(q, kv, indices, sm_scale, kv_format=KV_BF16, out=None, lse=None, device_buffer=None,
+                             chunk_tokens=256, device=None, stream=None):
+    """The forward from host (CPU) tensors, token chunks pipelined through the GPU (upload, compute and
+    download overlap).  Pinned tensors (``tensor.pin_memory()``) let the copies overlap; the call returns
+    when ``out`` and ``lse`` (host tensors) hold the result.  ``device_buffer`` is a uint8 CUDA tensor of at
+    least ``dsa_sparse_attn_fwd_host_device_bytes(...)`` bytes (allocated here when not given)."""
+    for name, t in (("q", q), ("kv", kv), ("indices", indices)):
+        if t.is_cuda:
+            raise ValueError(f"{name} must be a host tensor")
+    _check_shapes(q, kv, indices, kv_format)
+    lib = _lib.load()
+    s_q, h_q, _ = q.shape
+    s_kv, topk = kv.shape[0], indices.shape[1]
+    if out is None:
+        out = torch.empty((s_q, h_q, D_V), dtype=torch.bfloat16, pin_memory=q.is_pinned())
+    if lse is None:
+        lse = torch.empty((s_q, h_q), dtype=torch.float32, pin_memory=q.is_pinned())
+    if out.is_cuda or lse.is_cuda or out.dtype != torch.bfloat16 or lse.dtype != torch.float32 \
+            or tuple(out.shape) != (s_q, h_q, D_V) or tuple(lse.shape) != (s_q, h_q) \
+            or not out.is_contiguous() or not lse.is_contiguous():
+        raise ValueError("out / lse must be contiguous host tensors bf16 [s_q, h_q, 512] / f32 [s_q, h_q]")
+    need = int(lib.dsa_sparse_attn_fwd_host_device_bytes(kv_format, s_q, h_q, s_kv, topk, chunk_tokens))
+    if device_buffer is None and s_q > 0:
+        dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+        device_buffer = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    nbytes = device_buffer.numel() if device_buffer is not None else 0
+    st = lib.dsa_sparse_attn_fwd_host(kv_format, _ptr(q), _ptr(kv), _ptr(indices), s_q, h_q, s_kv, topk,
+                                      ctypes.c_float(sm_scale), _ptr(out), _ptr(lse), _ptr(device_buffer),
+                                      ctypes.c_size_t(nbytes), chunk_tokens, _stream_handle(stream))
+    if st != 0:
+        raise _lib.DsaError(st, "dsa_sparse_attn_fwd_host")
     return out, lse

@@ -82,3 +82,22 @@ def test_fp4_and_paged_host_validation_needs_no_device(lib):
     assert call(seq=ctypes.c_void_p(0x1002)) == 3             # int32 tables need 4-byte alignment
     assert call(s_q=0, seq=null, table=null) == 0             # nothing to do
     assert call() == 1                                        # passes the table checks, then null data pointers
+
+
+def test_host_pipeline_validation_needs_no_device(lib):
+    null = ctypes.c_void_p(0)
+    h = ctypes.c_void_p(0x1000)
+    f = lib.dsa_sparse_attn_fwd_host
+
+    def call(fmt=0, s_q=8, h_q=16, s_kv=64, topk=4, scale=0.1, chunk=4, ptr=h, buf=h, nbytes=1 << 30):
+        return f(fmt, ptr, ptr, ptr, s_q, h_q, s_kv, topk, ctypes.c_float(scale), ptr, ptr, buf,
+                 ctypes.c_size_t(nbytes), chunk, null)
+
+    assert call(fmt=3) == 1                       # unknown KV format
+    assert call(s_q=-1) == 1 and call(h_q=129) == 1 and call(topk=0) == 1 and call(chunk=0) == 1
+    assert call(scale=float("nan")) == 1
+    assert call(s_q=0, ptr=null, buf=null) == 0   # nothing to do
+    assert call(ptr=null) == 1                    # null host buffers
+    assert call() == 2                            # valid, but no sm_103 device here: no size, nothing launched
+    for bad in ((3, 8, 16, 64, 4, 4), (0, 0, 16, 64, 4, 4), (0, 8, 16, 64, 4, 0), (0, 8, 200, 64, 4, 4)):
+        assert lib.dsa_sparse_attn_fwd_host_device_bytes(*bad) == 0
