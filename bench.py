@@ -373,7 +373,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--s-q", type=int, default=4096, help="query tokens (4096 = the benchmark workload)")
     ap.add_argument("--skip-e2e", action="store_true")
-    ap.add_argument("--e2e-chunk", type=int, default=256,
+    ap.add_argument("--e2e-chunk", type=int, default=512,
                     help="query tokens per chunk of the host-buffer pipeline timed as e2e")
     ap.add_argument("--workload", default="prefill_causal",
                     choices=["prefill_causal", "decode_bf16", "decode_fp8", "long_prefill", "decode_paged",
