@@ -15,6 +15,8 @@ Modules:
               656-byte FP8 and 448-byte FP4 KV rows.
   paged       logical positions of a sequence -> rows of a paged KV pool
               through a block table (the forward itself is unchanged).
+  out_proj    the output projection with residual that follows the
+              attention, y = O . W_o + x, in float64.
 
 Every function is pinned by ``tests/test_oracle*.py`` against values fixed by
 the pages or by mathematics (closed forms, invariants, brute force, library
