@@ -139,12 +139,20 @@ def cpu_oracle_sample(wl, seconds: float, start_token: int = 0):
         from oracle import paged as PG
         idx = PG.logical_to_rows(idx, wl.meta["seq_of_token"].numpy(), wl.meta["block_table"].numpy(),
                                  wl.meta["page_size"], wl.kv.shape[0])
+    proj = wl.meta.get("w_o") is not None
+    if proj:  # the output projection with residual follows the forward
+        from oracle import out_proj as OP
+        wb = wl.meta["w_o"].contiguous().view(torch.int16).numpy().view(np.uint16)
+        xb = wl.meta["x"].contiguous().view(torch.int16).numpy().view(np.uint16)
     flops, n, t0 = 0.0, 0, time.perf_counter()
     t = start_token
     while True:
-        O.sparse_mla_fwd_sampled(qb, kvr, wl.kv_format, idx, wl.sm_scale, [t % wl.s_q])
+        o, _ = O.sparse_mla_fwd_sampled(qb, kvr, wl.kv_format, idx, wl.sm_scale, [t % wl.s_q])
         row = idx[t % wl.s_q]
         flops += 2.0 * wl.h_q * int(((row >= 0) & (row < wl.s_kv)).sum()) * 1088
+        if proj:
+            OP.out_proj_f64(o, wb, xb[t % wl.s_q:t % wl.s_q + 1])
+            flops += 2.0 * wb.shape[0] * wb.shape[1]
         n += 1
         t += 1
         if time.perf_counter() - t0 >= seconds or n >= wl.s_q:
@@ -218,6 +226,19 @@ def run_gb300(args, rank: int, world: int, local_rank: int):
             api.dsa_sparse_attn_fwd_paged(q, kv, idx, seq, table, wl.meta["page_size"], sm_scale, out=out, lse=lse,
                                           workspace=workspace)
 
+    proj, pflops = wl.meta.get("w_o") is not None, 0.0
+    if proj:  # forward, then y = out . W_o + x through the fused entry point
+        w_o, xres = wl.meta["w_o"].to(dev), wl.meta["x"].to(dev)
+        y = torch.empty_like(xres)
+        ws = torch.empty(api.dsa_sparse_attn_fwd_oproj_workspace_size(wl.s_q, wl.h_q, wl.topk, fmt),
+                         dtype=torch.uint8, device=dev)
+        pws = torch.empty(api.dsa_out_proj_workspace_size(), dtype=torch.uint8, device=dev)
+        pflops = 2.0 * wl.s_q * w_o.shape[0] * w_o.shape[1]
+
+        def fwd(q, kv, idx, sm_scale, out, lse, workspace):
+            api.dsa_sparse_attn_fwd_oproj(q, kv, idx, sm_scale, w_o, xres, kv_format=fmt, out=out, lse=lse, y=y,
+                                          workspace=workspace)
+
     def step():
         fwd(q, kv, idx, wl.sm_scale, out=out, lse=lse, workspace=ws)
 
@@ -252,6 +273,16 @@ def run_gb300(args, rank: int, world: int, local_rank: int):
     api.dsa_read_device_status(ws)
     step_ms = [a.elapsed_time(b) for a, b in ev]
     kern_ms = [a.elapsed_time(b) for a, b in kev]
+    proj_ms = None
+    if proj:  # the projection GEMM alone, same flush discipline
+        pe = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+        for i in range(K):
+            flush.zero_()
+            pe[i][0].record(stream)
+            api.dsa_out_proj(out, w_o, xres, y=y, workspace=pws)
+            pe[i][1].record(stream)
+        torch.cuda.synchronize()
+        proj_ms = sum(a.elapsed_time(b) for a, b in pe) / K
     ms = sum(step_ms) / K
     kms = sum(kern_ms) / K
     if world > 1:
@@ -262,19 +293,34 @@ def run_gb300(args, rank: int, world: int, local_rank: int):
     # ---- end to end through the public API from pinned host buffers
     e2e_ms = float('nan')
     if not args.skip_e2e:
-        e2e_ms = _e2e(args, wl, q, kv, idx, out, lse, step, stream, world, dev)
+        e2e_ms = _e2e(args, wl, q, kv, idx, out, lse, step, stream, world, dev,
+                      {"x": xres, "y": y} if proj else None)
 
     if rank != 0:
         return
-    return _report(args, wl, flops, ms, kms, e2e_ms, clocks, world)
+    return _report(args, wl, flops, ms, kms, e2e_ms, clocks, world, proj_ms, pflops)
 
 
-def _e2e(args, wl, q, kv, idx, out, lse, step, stream, world, dev):
+def _e2e(args, wl, q, kv, idx, out, lse, step, stream, world, dev, extra=None):
     qh, kvh, idxh = wl.q.pin_memory(), wl.kv.pin_memory(), wl.indices.pin_memory()
     outh = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     lseh = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
 
-    if wl.meta.get("paged"):
+    if wl.meta.get("w_o") is not None:
+        xh = wl.meta["x"].pin_memory()
+        yh = torch.empty(xh.shape, dtype=xh.dtype).pin_memory()
+
+        xd, yd = extra["x"], extra["y"]
+
+        def e2e_step():  # inputs and the residual in, y and lse out; W_o stays resident like model weights
+            q.copy_(qh, non_blocking=True)
+            kv.copy_(kvh, non_blocking=True)
+            idx.copy_(idxh, non_blocking=True)
+            xd.copy_(xh, non_blocking=True)
+            step()
+            yh.copy_(yd, non_blocking=True)
+            lseh.copy_(lse, non_blocking=True)
+    elif wl.meta.get("paged"):
         def e2e_step():  # the paged entry point takes device buffers: copies around it on one stream
             q.copy_(qh, non_blocking=True)
             kv.copy_(kvh, non_blocking=True)
@@ -312,11 +358,16 @@ def _e2e(args, wl, q, kv, idx, out, lse, step, stream, world, dev):
     return e2e_ms
 
 
-def _report(args, wl, flops, ms, kms, e2e_ms, clocks, world):
+def _report(args, wl, flops, ms, kms, e2e_ms, clocks, world, proj_ms=None, pflops=0.0):
+    """`flops` are the attention's (the roofline's kernel); `pflops` those of the output projection, if any."""
     from sparse_mla_attention_dsa_gb300 import api
     K = args.steps
+    proj = proj_ms is not None
     h2d = wl.q.numel() * 2 + wl.kv.numel() * wl.kv.element_size() + wl.indices.numel() * 4
     d2h = wl.s_q * wl.h_q * (512 * 2 + 4)
+    if proj:  # residual in; y and lse out (the attention output stays on the device)
+        h2d += wl.meta["x"].numel() * 2
+        d2h = wl.s_q * wl.h_q * 4 + wl.meta["x"].numel() * 2
     peak_tf, hbm_gbs, peak_src = _peaks()
     abytes = _alg_bytes(wl)
     t_flops, t_bytes = flops / (peak_tf * 1e12), abytes / (hbm_gbs * 1e9)
@@ -335,7 +386,8 @@ def _report(args, wl, flops, ms, kms, e2e_ms, clocks, world):
                  "kernel": "dsa_fwd_kernel<%d>" % {"bf16": 0, "fp8": 1, "fp4": 2}[wl.kv_format],
                  "kernel_ms": kms, "tensor_frac": tf_achieved / peak_tf, "hbm_frac": gbs_achieved / hbm_gbs,
                  "roofline_ms": 1e3 * max(t_flops, t_bytes)})
-    value = world * flops / (ms * 1e-3) / 1e12
+    total = flops + pflops
+    value = world * total / (ms * 1e-3) / 1e12
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
             "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic",
@@ -345,15 +397,22 @@ def _report(args, wl, flops, ms, kms, e2e_ms, clocks, world):
                        "l2": "flushed before every step (270 MB write, outside the step events)",
                        "parallelism": f"replicas x{world} (tokens are independent)"},
             "roofline": roof,
-            "e2e": None if args.skip_e2e else {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+            "e2e": None if args.skip_e2e else {"value": world * total / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
                                                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                                                "ms_per_step": e2e_ms,
-                                               "api": "dsa_sparse_attn_fwd_paged + torch copies"
+                                               "api": "dsa_sparse_attn_fwd_oproj + torch copies" if proj
+                                               else "dsa_sparse_attn_fwd_paged + torch copies"
                                                if wl.meta.get("paged") else "dsa_sparse_attn_fwd_host",
-                                               "chunk_tokens": None if wl.meta.get("paged")
+                                               "chunk_tokens": None if (proj or wl.meta.get("paged"))
                                                else min(args.e2e_chunk, wl.s_q)},
             "gpu_launches": K * api.dsa_kernels_per_call(),
             "clocks": clocks}
+    if proj:
+        line["config"]["d_model"] = wl.meta["d_model"]
+        line["config"]["step"] = "forward, then y = out . W_o + x (cuBLASLt GEMM, not counted in gpu_launches)"
+        line["out_proj"] = {"ms": proj_ms, "tflops": pflops / (proj_ms * 1e-3) / 1e12,
+                            "tensor_frac": pflops / (proj_ms * 1e-3) / 1e12 / peak_tf, "flops": pflops,
+                            "gemm": f"bf16 M={wl.s_q} K={wl.h_q * 512} N={wl.meta['d_model']}, fp32 accumulate"}
     if not args.no_cpu_baseline:
         f, dt, n = cpu_oracle_sample(wl, args.cpu_seconds)
         line["cpu_baseline"] = {"value": f / dt / 1e12, "unit": UNIT, "cores": host_cores(), "kind": "oracle",
@@ -377,7 +436,7 @@ def main():
                     help="query tokens per chunk of the host-buffer pipeline timed as e2e")
     ap.add_argument("--workload", default="prefill_causal",
                     choices=["prefill_causal", "decode_bf16", "decode_fp8", "long_prefill", "decode_paged",
-                             "decode_fp4", "tiny"])
+                             "decode_fp4", "prefill_oproj", "tiny"])
     ap.add_argument("--traffic", type=float, default=None,
                     help="DRAM bytes per attention-kernel launch from an ncu capture (null when not given)")
     args = ap.parse_args()

@@ -198,6 +198,35 @@ DSA_API dsa_status dsa_sparse_attn_fwd_host(int kv_format, const void* q_host, c
                                             float sm_scale, void* out_host, float* lse_host, void* device_buffer,
                                             size_t device_bytes, int chunk_tokens, cudaStream_t stream);
 
+/* Output projection with residual after the attention
+ * ("FlashMLA算子Ascend 950移植：从tiling到访存优化全解读", section 3.4, 输出投影与残差合并):
+ *   y[t, :] = O[t, :] . W_o + x[t, :]
+ * where O[t, :] is the head-major concatenation of the attention output, i.e. the bf16 `out`
+ * [s_q, h_q, 512] of a forward read as [s_q, h_q * 512].
+ *   o          bf16 [s_q, h_q * 512] (the forward's `out`)
+ *   w_o        bf16 [h_q * 512, d_model], row-major
+ *   x          bf16 [s_q, d_model] residual, or NULL for none; may equal y (in place)
+ *   y          bf16 [s_q, d_model] output (fp32 accumulation, rounded to nearest even)
+ *   workspace  >= dsa_out_proj_workspace_size() bytes of device memory, 16-byte aligned
+ * d_model must be a multiple of 8 (>= 8) and 1 <= h_q <= 128; all pointers 16-byte aligned.  Runs as
+ * one cuBLASLt GEMM on `stream` (asynchronous).  The library keeps one cuBLASLt handle per device and
+ * a cache of the chosen algorithm per shape for the life of the process.  Returns DSA_ERR_INVALID_ARG,
+ * DSA_ERR_MISALIGNED or DSA_ERR_WORKSPACE before any work for bad arguments, DSA_ERR_UNSUPPORTED if no
+ * GEMM algorithm fits, DSA_ERR_CUDA if the GEMM launch failed. */
+DSA_API size_t dsa_out_proj_workspace_size(void);
+DSA_API dsa_status dsa_out_proj(const void* o, const void* w_o, const void* x, int s_q, int h_q, int d_model,
+                                void* y, void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* The forward followed by the output projection on the same stream: out and lse as for the
+ * kv_format's forward entry point, then y = out . W_o + x as dsa_out_proj.  The workspace holds the
+ * forward's workspace (first, so dsa_read_device_status reads it) and the GEMM's:
+ * dsa_sparse_attn_fwd_oproj_workspace_size(s_q, h_q, topk, kv_format) bytes. */
+DSA_API size_t dsa_sparse_attn_fwd_oproj_workspace_size(int s_q, int h_q, int topk, int kv_format);
+DSA_API dsa_status dsa_sparse_attn_fwd_oproj(int kv_format, const void* q, const void* kv, const int32_t* indices,
+                                             int s_q, int h_q, int s_kv, int topk, float sm_scale, const void* w_o,
+                                             const void* x, int d_model, void* out, float* lse, void* y,
+                                             void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
 /* Synchronises `stream` and returns the device-side status a previous forward
  * call left in `workspace` (DSA_OK or DSA_ERR_DEVICE_TIMEOUT), or DSA_ERR_CUDA
  * if the synchronisation itself failed. */

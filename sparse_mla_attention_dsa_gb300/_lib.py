@@ -24,6 +24,10 @@ SIGNATURES = {
     "dsa_sparse_attn_fwd_paged": (_I, [_I, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P, _S, _P]),
     "dsa_sparse_attn_fwd_host_device_bytes": (_S, [_I, _I, _I, _I, _I, _I]),
     "dsa_sparse_attn_fwd_host": (_I, [_I, _P, _P, _P, _I, _I, _I, _I, _F, _P, _P, _P, _S, _I, _P]),
+    "dsa_out_proj_workspace_size": (_S, []),
+    "dsa_out_proj": (_I, [_P, _P, _P, _I, _I, _I, _P, _P, _S, _P]),
+    "dsa_sparse_attn_fwd_oproj_workspace_size": (_S, [_I, _I, _I, _I]),
+    "dsa_sparse_attn_fwd_oproj": (_I, [_I, _P, _P, _P, _I, _I, _I, _I, _F, _P, _P, _I, _P, _P, _P, _P, _S, _P]),
 }
 
 STATUS = {0: "DSA_OK", 1: "DSA_ERR_INVALID_ARG", 2: "DSA_ERR_UNSUPPORTED", 3: "DSA_ERR_MISALIGNED", 4: "DSA_ERR_CUDA",

@@ -215,3 +215,67 @@ def dsa_sparse_attn_fwd_host(q, kv, indices, sm_scale, kv_format=KV_BF16, out=No
     if st != 0:
         raise _lib.DsaError(st, "dsa_sparse_attn_fwd_host")
     return out, lse
+
+
+def dsa_out_proj(out, w_o, x=None, y=None, workspace=None, stream=None):
+    """y = out . W_o + x: out bf16 [s_q, h_q, 512] (a forward's output), w_o bf16 [h_q * 512, d_model],
+    x bf16 [s_q, d_model] or None.  Returns y bf16 [s_q, d_model]."""
+    s_q, h_q = out.shape[0], out.shape[1]
+    d_model = w_o.shape[1]
+    _check_oproj(out, w_o, x, s_q, h_q, d_model)
+    lib = _lib.load()
+    if y is None:
+        y = torch.empty((s_q, d_model), dtype=torch.bfloat16, device=out.device)
+    if workspace is None:
+        workspace = torch.empty(dsa_out_proj_workspace_size(), dtype=torch.uint8, device=out.device)
+    st = lib.dsa_out_proj(_ptr(out), _ptr(w_o), _ptr(x), s_q, h_q, d_model, _ptr(y), _ptr(workspace),
+                          ctypes.c_size_t(workspace.numel()), _stream_handle(stream))
+    if st != 0:
+        raise _lib.DsaError(st, "dsa_out_proj")
+    return y
+
+
+def _check_oproj(out, w_o, x, s_q, h_q, d_model):
+    if out.dtype != torch.bfloat16 or out.dim() != 3 or out.shape[2] != D_V or not out.is_contiguous():
+        raise ValueError("out must be a contiguous bf16 tensor [s_q, h_q, 512]")
+    if w_o.dtype != torch.bfloat16 or w_o.dim() != 2 or w_o.shape[0] != h_q * D_V or not w_o.is_contiguous():
+        raise ValueError("w_o must be a contiguous bf16 tensor [h_q * 512, d_model]")
+    if x is not None and (x.dtype != torch.bfloat16 or tuple(x.shape) != (s_q, d_model) or not x.is_contiguous()):
+        raise ValueError("x must be a contiguous bf16 tensor [s_q, d_model]")
+
+
+def dsa_sparse_attn_fwd_oproj(q, kv, indices, sm_scale, w_o, x=None, kv_format=KV_BF16, out=None, lse=None, y=None,
+                              workspace=None, stream=None, check_status=False):
+    """The forward, then y = out . W_o + x on the same stream.  Returns (y, out, lse)."""
+    _check(q, kv, indices, kv_format)
+    lib = _lib.load()
+    s_q, h_q, _ = q.shape
+    topk = indices.shape[1]
+    d_model = w_o.shape[1]
+    if out is None:
+        out = torch.empty((s_q, h_q, D_V), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((s_q, h_q), dtype=torch.float32, device=q.device)
+    if y is None:
+        y = torch.empty((s_q, d_model), dtype=torch.bfloat16, device=q.device)
+    _check_oproj(out, w_o, x, s_q, h_q, d_model)
+    if workspace is None:
+        nb = int(lib.dsa_sparse_attn_fwd_oproj_workspace_size(s_q, h_q, topk, kv_format))
+        workspace = torch.empty(max(nb, 256), dtype=torch.uint8, device=q.device)
+    st = lib.dsa_sparse_attn_fwd_oproj(kv_format, _ptr(q), _ptr(kv), _ptr(indices), s_q, h_q, kv.shape[0], topk,
+                                       ctypes.c_float(sm_scale), _ptr(w_o), _ptr(x), d_model, _ptr(out), _ptr(lse),
+                                       _ptr(y), _ptr(workspace), ctypes.c_size_t(workspace.numel()),
+                                       _stream_handle(stream))
+    if st != 0:
+        raise _lib.DsaError(st, "dsa_sparse_attn_fwd_oproj")
+    if check_status:
+        dsa_read_device_status(workspace, stream)
+    return y, out, lse
+
+
+def dsa_sparse_attn_fwd_oproj_workspace_size(s_q: int, h_q: int, topk: int, kv_format: int = KV_BF16) -> int:
+    return int(_lib.load().dsa_sparse_attn_fwd_oproj_workspace_size(s_q, h_q, topk, kv_format))
+
+
+def dsa_out_proj_workspace_size() -> int:
+    return int(_lib.load().dsa_out_proj_workspace_size())

@@ -18,7 +18,7 @@ CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB_NAME = "libdsa_gb300.so"
 LIB_PATH = os.path.join(OUT_DIR, LIB_NAME)
-SOURCES = ["dsa_api.cu", "dsa_fwd.cu", "dsa_fwd_fp8.cu", "dsa_fwd_fp4.cu", "dsa_noalloc.cu", "dsa_host.cu"]
+SOURCES = ["dsa_api.cu", "dsa_fwd.cu", "dsa_fwd_fp8.cu", "dsa_fwd_fp4.cu", "dsa_noalloc.cu", "dsa_host.cu", "dsa_oproj.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
                      "--expt-relaxed-constexpr"]
@@ -65,7 +65,7 @@ def build(verbose: bool = False, force: bool = False, extra_flags=()) -> str:
     with ThreadPoolExecutor(max_workers=len(jobs) or 1) as ex:
         list(ex.map(run, jobs))
     if force or jobs or _stale(LIB_PATH, objs):
-        cmd = [nvcc, *ARCH, "-shared", "-Xcompiler", "-fPIC", "-o", LIB_PATH, *objs]
+        cmd = [nvcc, *ARCH, "-shared", "-Xcompiler", "-fPIC", "-o", LIB_PATH, *objs, "-lcublasLt"]
         run(cmd)
     return LIB_PATH
 

@@ -358,3 +358,34 @@ def decode_fp4(seed: int = 6, n_seq: int = 128, h_q: int = 128, s_kv_per_seq: in
 
 WORKLOADS["decode_paged"] = decode_paged
 WORKLOADS["decode_fp4"] = decode_fp4
+
+
+# ---------------------------------------------------------------- output projection inputs
+D_MODEL = 7168  # hidden size of the model the projection writes into (DeepSeek-V3's)
+
+
+def oproj_inputs(seed: int, s_q: int, h_q: int, d_model: int = D_MODEL, out_sigma: float = 0.05):
+    """Synthetic weights and residual for y = O . W_o + x: W_o bf16 [h_q * 512, d_model] ~ N(0, 1/sqrt(h_q * 512))
+    (so that y has the scale of one attention output value), x bf16 [s_q, d_model] ~ N(0, 1), and a stand-alone
+    attention output O bf16 [s_q, h_q, 512] ~ N(0, out_sigma) for tests of the projection alone."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    k = h_q * D_V
+    w_o = _normal_bf16(rng, (k, d_model), sigma=1.0 / math.sqrt(k))
+    x = _normal_bf16(rng, (s_q, d_model))
+    o = _normal_bf16(rng, (s_q, h_q, D_V), sigma=out_sigma)
+    return w_o, x, o
+
+
+def prefill_oproj(seed: int = 7, d_model: int = D_MODEL) -> Workload:
+    """The causal prefill followed by the output projection with residual into a d_model-wide hidden state."""
+    wl = prefill_causal()
+    rng = np.random.Generator(np.random.PCG64(seed))
+    k = wl.h_q * D_V
+    w_o = _normal_bf16(rng, (k, d_model), sigma=1.0 / math.sqrt(k))
+    x = _normal_bf16(rng, (wl.s_q, d_model))
+    wl.name = "prefill_oproj"
+    wl.meta.update({"w_o": w_o, "x": x, "d_model": d_model})
+    return wl
+
+
+WORKLOADS["prefill_oproj"] = prefill_oproj
