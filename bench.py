@@ -65,7 +65,8 @@ def _peaks():
 
 
 class ClockSampler:
-    """nvidia-smi samples every 20 ms while the timed region runs."""
+    """nvidia-smi samples every 20 ms while the timed region runs, plus the last sample before it (a region
+    shorter than the interval is bracketed by the samples just before and after)."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -81,7 +82,25 @@ class ClockSampler:
         except (FileNotFoundError, OSError):
             self.proc = None
 
-    def stop(self):
+    def _rows(self):
+        self.f.flush()
+        with open(self.f.name) as g:
+            return [r for r in g.read().strip().splitlines() if r.count(",") >= 8]
+
+    def wait_rows(self, n: int, timeout: float = 3.0) -> None:
+        """Block until the sampler has written at least n rows (or timeout)."""
+        if self.proc is None:
+            return
+        t0 = time.perf_counter()
+        while len(self._rows()) < n and time.perf_counter() - t0 < timeout:
+            time.sleep(0.005)
+
+    def mark(self) -> int:
+        return len(self._rows()) if self.proc is not None else 0
+
+    def stop(self, first: int = 0):
+        """Rows from index `first` on (the caller marks the last row written before its timed region; for a
+        region shorter than the sampling interval the rows just before and after bracket it)."""
         if self.proc is None:
             return None
         self.proc.terminate()
@@ -91,7 +110,7 @@ class ClockSampler:
             self.proc.kill()
         self.f.flush()
         self.f.seek(0)
-        rows = [r.split(",") for r in self.f.read().strip().splitlines() if r.count(",") >= 8]
+        rows = [r.split(",") for r in self.f.read().strip().splitlines() if r.count(",") >= 8][max(0, first - 1):]
         os.unlink(self.f.name)
         if not rows:
             return None
@@ -256,6 +275,8 @@ def run_gb300(args, rank: int, world: int, local_rank: int):
         a.record(stream)
         b.record(stream)
     sampler = ClockSampler(local_rank)
+    sampler.wait_rows(1)  # sampling runs before the region starts
+    first_row = sampler.mark()
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
@@ -269,7 +290,8 @@ def run_gb300(args, rank: int, world: int, local_rank: int):
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
-    clocks = sampler.stop()
+    sampler.wait_rows(first_row + 1)  # at least one sample at or after the region's end
+    clocks = sampler.stop(first_row)
     api.dsa_read_device_status(ws)
     step_ms = [a.elapsed_time(b) for a, b in ev]
     kern_ms = [a.elapsed_time(b) for a, b in kev]

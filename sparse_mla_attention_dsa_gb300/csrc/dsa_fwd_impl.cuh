@@ -698,6 +698,14 @@ __device__ void qk_softmax(const Ctx& c, const FwdParams& p) {
     if (!wait(c, A_Q_FREE, (item & 1u) ^ 1u)) { ok = false; break; }
     tc_fence_after();
     {
+      // this thread's share of the next token's Q row moves into L2 now, one token of work before the
+      // next piece reads it (the Q load at a token switch stalls the QK tensor core)
+      if (pc.t + 1 < p.s_q && r < p.h_q) {
+        const uint8_t* nq = (const uint8_t*)(p.q + ((size_t)(pc.t + 1) * p.h_q + r) * kDQK);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) prefetch_l2(nq + half * 512 + u * 128);
+        if (half == 0) prefetch_l2(nq + 1024);
+      }
       const bool live = r < p.h_q;
       const uint4* qrow = (const uint4*)(p.q + ((size_t)pc.t * p.h_q + (live ? r : 0)) * kDQK);
 #pragma unroll 1
