@@ -33,12 +33,15 @@
 //
 // Warp roles (512 threads, both CTAs): warp 0 compacts the valid indices of
 // each block into a small ring of index lists; warp 2 issues tcgen05.mma;
-// warp 3 owns the TMEM allocation (and, on the PV side, returns P slots to
-// the QK side).  QK side: warps 4-11 run the softmax (warp w serves TMEM lane
-// quarter w % 4 and column half (w - 4) / 4), warps 1 and 12-15 gather.  PV
-// side: warps 4-7 rescale O and run the epilogue (one TMEM lane quarter each),
-// warps 1 and 8-15 gather.  Gathering gets many warps because a GB300 SM
-// ingests random 128-byte row pieces at only a few tens of bytes per clock.
+// warp 3 allocates TMEM.  QK side: warps 4-11 run the softmax (warp w serves
+// TMEM lane quarter w % 4 and column half (w - 4) / 4).  PV side: warps 4-7
+// rescale O and run the epilogue (one TMEM lane quarter each), warp 3 returns
+// P slots to the QK side.  The gather: bf16 rows come by one bulk copy per row
+// (QK: warps 12-15 issue, warps 1 and 3 transpose; PV: warps 8-13 issue,
+// warps 1, 14, 15 transpose); quantised rows come by cp.async and are
+// dequantised by the same warps (QK: 1, 3, 12-15; PV: 1, 8-15).  Gathering
+// gets many warps because a GB300 SM ingests random row pieces at only a few
+// tens of bytes per clock.
 #pragma once
 #include <cuda_fp16.h>
 #include <cuda_fp4.h>
@@ -59,7 +62,7 @@ constexpr int kFmtBf16 = 0, kFmtFp8 = 1, kFmtFp4 = 2;
 constexpr int kThreads = 512;
 constexpr int kSoftmaxWarps = 8;                 // QK side, warps 4..11
 constexpr int kEpiWarps = 4;                     // PV side, warps 4..7
-constexpr int kGatherWarpsA = 5;                 // FP8, QK side: warps 1, 12..15
+constexpr int kGatherWarpsA = 6;                 // FP8, QK side: warps 1, 3, 12..15
 constexpr int kGatherWarpsB = 9;                 // FP8, PV side: warps 1, 8..15
 // bf16 rows: bulk-copy issuers and in-place transposers
 constexpr int kIssuersA = 4;                     // QK side: warps 12..15
@@ -439,7 +442,7 @@ static __device__ void qk_gather_q(const Ctx& c, const FwdParams& p) {
   using R = QRow<kFmt>;
   uint8_t* smem = c.smem;
   const int warp = c.warp, lane = c.lane;
-  const int gw = (warp == 1) ? 0 : warp - 11;  // 0..4
+  const int gw = (warp == 1) ? 0 : (warp == 3) ? 5 : warp - 11;  // 0..5
   const int gt = gw * 32 + lane;
   constexpr int kGT = kGatherWarpsA * 32;
   const int* lists = (const int*)(smem + Y::OffIdx);
@@ -1211,7 +1214,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(fwd::kThreads, 1) ds
     else pv_mma<kFmt>(c, p);
   } else if (c.rank == 0) {
     if constexpr (kQuant) {
-      if (w == 1 || w >= 12) qk_gather_q<kFmt>(c, p);
+      if (w == 1 || w == 3 || w >= 12) qk_gather_q<kFmt>(c, p);
       else if (w >= 4) qk_softmax<kFmt>(c, p);
     } else {
       if (w >= 12) qk_issue_bf16(c, p);
