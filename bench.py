@@ -39,7 +39,6 @@ import torch  # noqa: E402
 
 METRIC = "sparse MLA fwd TFLOPS & % of roofline (h_q=128, topk=2048, 1×GB300)"
 UNIT = "TFLOP/s"
-WORKLOAD = "prefill_causal"
 L2_FLUSH_BYTES = 2 * 135_528_448  # twice the GB300 L2
 
 
@@ -186,12 +185,22 @@ def host_cores() -> int:
         return os.cpu_count() or 1
 
 
+def max_over_ranks(values, world: int, dev) -> list:
+    """Element-wise maximum of per-rank timings over all ranks (the slowest rank sets the job's time); the
+    identity for one rank.  Needs an initialised process group when world > 1."""
+    if world <= 1:
+        return [float(v) for v in values]
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=dev)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
 def run_reference(args, rank: int, world: int):
-    """The CPU oracle as it stands, on this host's cores, each step a bounded token sample."""
+    """The CPU oracle as it stands, on this host's cores, each step a bounded token sample (rank 0 only)."""
     from sparse_mla_attention_dsa_gb300 import workloads as W
     if rank != 0:
         return
-    wl = W.prefill_causal()
+    wl = W.WORKLOADS[args.workload]() if args.workload != "prefill_causal" else W.prefill_causal()
     for w in range(args.warmup):
         cpu_oracle_sample(wl, 0.0, start_token=w)
     times, flops_all, ntok = [], 0.0, 0
@@ -207,10 +216,11 @@ def run_reference(args, rank: int, world: int):
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
-            "config": {"workload": WORKLOAD, "s_q": wl.s_q, "h_q": wl.h_q, "s_kv": wl.s_kv, "topk": wl.topk,
-                       "n_valid_per_token": 1946, "step": f"~{args.ref_step_seconds:g} s token sample"},
+            "config": {"workload": args.workload, "s_q": wl.s_q, "h_q": wl.h_q, "s_kv": wl.s_kv, "topk": wl.topk,
+                       "n_valid_per_token": round(flops_all / max(ntok, 1) / (2 * wl.h_q * 1088), 1),
+                       "step": f"~{args.ref_step_seconds:g} s token sample"},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": host_cores(), "kind": "oracle",
-                             "sample": f"{ntok} tokens of {WORKLOAD} over {args.steps} steps (numpy float64, "
+                             "sample": f"{ntok} tokens of {args.workload} over {args.steps} steps (numpy float64, "
                                        f"BLAS threads = host cores)"},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -307,10 +317,9 @@ def run_gb300(args, rank: int, world: int, local_rank: int):
         proj_ms = sum(a.elapsed_time(b) for a, b in pe) / K
     ms = sum(step_ms) / K
     kms = sum(kern_ms) / K
-    if world > 1:
-        t = torch.tensor([ms, kms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms, kms = float(t[0]), float(t[1])
+    ms, kms = max_over_ranks([ms, kms], world, dev)
+    if proj_ms is not None:
+        proj_ms = max_over_ranks([proj_ms], world, dev)[0]
 
     # ---- end to end through the public API from pinned host buffers
     e2e_ms = float('nan')
@@ -371,11 +380,7 @@ def _e2e(args, wl, q, kv, idx, out, lse, step, stream, world, dev, extra=None):
         e2e_step()
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / KE
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t[0])
+    e2e_ms = max_over_ranks([e0.elapsed_time(e1) / KE], world, dev)[0]
 
     return e2e_ms
 
