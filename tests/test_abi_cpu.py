@@ -101,3 +101,26 @@ def test_host_pipeline_validation_needs_no_device(lib):
     assert call() == 2                            # valid, but no sm_103 device here: no size, nothing launched
     for bad in ((3, 8, 16, 64, 4, 4), (0, 0, 16, 64, 4, 4), (0, 8, 16, 64, 4, 0), (0, 8, 200, 64, 4, 4)):
         assert lib.dsa_sparse_attn_fwd_host_device_bytes(*bad) == 0
+
+
+def test_projection_validation_needs_no_device(lib):
+    null = ctypes.c_void_p(0)
+    h = ctypes.c_void_p(0x1000)
+    f = lib.dsa_out_proj
+    ws = lib.dsa_out_proj_workspace_size()
+    assert ws >= (1 << 20)
+
+    def call(s_q=4, h_q=2, d_model=16, o=h, w=h, x=null, y=h, buf=h, nbytes=ws):
+        return f(o, w, x, s_q, h_q, d_model, y, buf, ctypes.c_size_t(nbytes), null)
+
+    assert call(s_q=0, o=null, w=null, y=null, buf=null) == 0      # nothing to do
+    assert call(d_model=12) == 1 and call(d_model=0) == 1 and call(h_q=0) == 1 and call(h_q=129) == 1
+    assert call(s_q=-1) == 1 and call(o=null) == 1 and call(y=null) == 1
+    assert call(x=ctypes.c_void_p(0x1008)) == 3                     # residual not 16-byte aligned
+    assert call(nbytes=ws - 1) == 6 and call(buf=null) == 6          # workspace
+    fused = lib.dsa_sparse_attn_fwd_oproj
+    args = [null, null, null, 2, 16, 10, 4, ctypes.c_float(0.1), h, null, 16, h, h, h, h, ctypes.c_size_t(1 << 30), null]
+    assert fused(3, *args) == 1                                      # unknown KV format
+    bad_d = list(args); bad_d[10] = 20
+    assert fused(0, *bad_d) == 1                                     # d_model not a multiple of 8
+    assert fused(0, *args) == 2                                      # valid, but no sm_103 device here
