@@ -21,10 +21,14 @@
  * with no valid slot gets out = 0 and lse = -inf.  Slot order does not change
  * the result beyond rounding.
  *
- * Memory: every pointer is a DEVICE pointer owned by the caller.  The library
- * allocates nothing and keeps no per-call state outside the caller's
- * workspace.  All calls are asynchronous on `stream`; their return value
- * reports host-side validation and launch errors only.  A device-side failure
+ * Memory: every pointer is a DEVICE pointer owned by the caller, except in
+ * dsa_sparse_attn_fwd_host (host buffers in and out).  The library allocates no
+ * device memory and keeps no per-call state outside the caller's workspace; the
+ * exceptions are stated at dsa_sparse_attn_fwd_host (its own copy streams and
+ * events for the length of the call), dsa_sparse_attn_fwd_noalloc (a built-in
+ * scratch array) and dsa_out_proj (a cuBLASLt handle and algorithm cache).
+ * All calls but dsa_sparse_attn_fwd_host are asynchronous on `stream`; their
+ * return value reports host-side validation and launch errors only.  A device-side failure
  * (a bounded wait inside a kernel that gave up) is written to the workspace
  * and read back with dsa_read_device_status().  No call aborts or throws.
  *
@@ -184,7 +188,9 @@ DSA_API dsa_status dsa_sparse_attn_fwd_fp4kv(const void* q, const void* kv_fp4, 
  *                  s_kv, topk, chunk_tokens) bytes of device memory, 16-byte
  *                  aligned, owned by the caller; it holds the whole KV, two sets of
  *                  chunk buffers and a workspace, and its contents are scratch.
- *   chunk_tokens   tokens per chunk, >= 1 (s_q or more: one chunk, no overlap).
+ *   chunk_tokens   tokens per chunk, >= 1 (s_q or more: one chunk, no overlap); when there are
+ *                  several, the first and the last hold half as many, which shortens the upload
+ *                  before the first forward and the download after the last one.
  * The work is queued after what `stream` already holds and the call returns
  * when out_host and lse_host hold the result (it synchronises).  Returns
  * DSA_ERR_INVALID_ARG / DSA_ERR_WORKSPACE / DSA_ERR_UNSUPPORTED before any

@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <utility>
 #include <vector>
 
 #include "../../include/dsa.h"
@@ -23,11 +24,39 @@ struct HostLayout {
   size_t status, ws, ws_bytes, kv, q[2], idx[2], out[2], lse[2], total;
 };
 
+// Token ranges of the chunks: the first and the last chunk are half size, so that the upload before the
+// first forward and the download after the last one (the parts no compute hides) are short; the rest are
+// `chunk` tokens.  One chunk when s_q <= chunk.
+std::vector<std::pair<int, int>> chunk_plan(int s_q, int chunk) {
+  std::vector<std::pair<int, int>> v;
+  if (s_q <= chunk) {
+    v.emplace_back(0, s_q);
+    return v;
+  }
+  const int half = chunk / 2 > 0 ? chunk / 2 : 1;
+  int t = 0;
+  v.emplace_back(t, half);
+  t += half;
+  while (s_q - t > chunk + half) {
+    v.emplace_back(t, chunk);
+    t += chunk;
+  }
+  const int rest = s_q - t;  // in (0, chunk + half]
+  if (rest > half) {
+    v.emplace_back(t, rest - half);
+    t += rest - half;
+    v.emplace_back(t, half);
+  } else {
+    v.emplace_back(t, rest);
+  }
+  return v;
+}
+
 // Device buffer: one status word per chunk, the forward workspace, the whole KV, then two sets of chunk
 // buffers (q, indices, out, lse).  Every region starts on a 256-byte boundary.
 HostLayout host_layout(int kv_format, int s_q, int h_q, int s_kv, int topk, int chunk) {
   HostLayout L{};
-  const int nchunks = (s_q + chunk - 1) / chunk;
+  const int nchunks = (int)chunk_plan(s_q, chunk).size();
   size_t off = 0;
   L.status = off; off += up(sizeof(int) * (size_t)nchunks);
   L.ws = off;
@@ -114,7 +143,8 @@ dsa_status dsa_sparse_attn_fwd_host(int kv_format, const void* q_host, const voi
   int* status_dev = reinterpret_cast<int*>(dev + L.status);
   const size_t q_tok = (size_t)h_q * DSA_D_QK * 2, idx_tok = (size_t)topk * sizeof(int32_t),
                out_tok = (size_t)h_q * DSA_D_V * 2, lse_tok = (size_t)h_q * sizeof(float);
-  const int nchunks = (s_q + chunk - 1) / chunk;
+  const std::vector<std::pair<int, int>> plan = chunk_plan(s_q, chunk);
+  const int nchunks = (int)plan.size();
   auto ck = [](cudaError_t e) { return e == cudaSuccess; };
   dsa_status result = DSA_OK;
   bool ok = true;
@@ -127,7 +157,7 @@ dsa_status dsa_sparse_attn_fwd_host(int kv_format, const void* q_host, const voi
   ok &= ck(cudaEventRecord(pp.kv, pp.h2d));
   ok &= ck(cudaStreamWaitEvent(stream, pp.kv, 0));
   for (int i = 0; i < nchunks && ok; ++i) {
-    const int b = i & 1, t0 = i * chunk, n = (s_q - t0) < chunk ? (s_q - t0) : chunk;
+    const int b = i & 1, t0 = plan[(size_t)i].first, n = plan[(size_t)i].second;
     // inputs of chunk i into buffer set b once chunk i-2's forward has read it
     if (i >= 2) ok &= ck(cudaStreamWaitEvent(pp.h2d, pp.comp[b], 0));
     ok &= ck(cudaMemcpyAsync(dev + L.q[b], static_cast<const uint8_t*>(q_host) + t0 * q_tok, n * q_tok,
