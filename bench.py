@@ -54,6 +54,18 @@ def _alg_bytes(wl) -> float:
     return nv * row + wl.s_q * wl.h_q * (576 * 2 + 512 * 2 + 4) + wl.indices.numel() * 4
 
 
+def _compulsory_bytes(wl) -> float:
+    """Bytes that must cross HBM once: every distinct KV row that some token selects, Q, out, lse, indices."""
+    idx = wl.indices.flatten()
+    ok = (idx >= 0) & (idx < wl.s_kv)
+    if wl.meta.get("paged"):
+        uniq = wl.kv.shape[0]  # upper bound: the whole pool (the translation is not redone here)
+    else:
+        uniq = int(torch.unique(idx[ok]).numel())
+    row = {"bf16": 1152, "fp8": 656, "fp4": 448}[wl.kv_format]
+    return uniq * row + wl.s_q * wl.h_q * (576 * 2 + 512 * 2 + 4) + wl.indices.numel() * 4
+
+
 def _peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -306,6 +318,14 @@ def run_gb300(args, rank: int, world: int, local_rank: int):
     step_ms = [a.elapsed_time(b) for a, b in ev]
     kern_ms = [a.elapsed_time(b) for a, b in kev]
     proj_ms = None
+    # the same steps with the L2 left warm (no flush between them), for reference
+    wev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    for i in range(K):
+        wev[i][0].record(stream)
+        step()
+        wev[i][1].record(stream)
+    torch.cuda.synchronize()
+    warm_ms = max_over_ranks([sum(a.elapsed_time(b) for a, b in wev) / K], world, dev)[0]
     if proj:  # the projection GEMM alone, same flush discipline
         pe = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
         for i in range(K):
@@ -329,7 +349,7 @@ def run_gb300(args, rank: int, world: int, local_rank: int):
 
     if rank != 0:
         return
-    return _report(args, wl, flops, ms, kms, e2e_ms, clocks, world, proj_ms, pflops)
+    return _report(args, wl, flops, ms, kms, e2e_ms, clocks, world, proj_ms, pflops, warm_ms)
 
 
 def _e2e(args, wl, q, kv, idx, out, lse, step, stream, world, dev, extra=None):
@@ -385,7 +405,7 @@ def _e2e(args, wl, q, kv, idx, out, lse, step, stream, world, dev, extra=None):
     return e2e_ms
 
 
-def _report(args, wl, flops, ms, kms, e2e_ms, clocks, world, proj_ms=None, pflops=0.0):
+def _report(args, wl, flops, ms, kms, e2e_ms, clocks, world, proj_ms=None, pflops=0.0, warm_ms=None):
     """`flops` are the attention's (the roofline's kernel); `pflops` those of the output projection, if any."""
     from sparse_mla_attention_dsa_gb300 import api
     K = args.steps
@@ -413,6 +433,8 @@ def _report(args, wl, flops, ms, kms, e2e_ms, clocks, world, proj_ms=None, pflop
                  "kernel": "dsa_fwd_kernel<%d>" % {"bf16": 0, "fp8": 1, "fp4": 2}[wl.kv_format],
                  "kernel_ms": kms, "tensor_frac": tf_achieved / peak_tf, "hbm_frac": gbs_achieved / hbm_gbs,
                  "roofline_ms": 1e3 * max(t_flops, t_bytes)})
+    cbytes = _compulsory_bytes(wl)
+    roof.update({"compulsory_bytes": cbytes, "compulsory_ms": 1e3 * cbytes / (hbm_gbs * 1e9)})
     total = flops + pflops
     value = world * total / (ms * 1e-3) / 1e12
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
@@ -434,6 +456,9 @@ def _report(args, wl, flops, ms, kms, e2e_ms, clocks, world, proj_ms=None, pflop
                                                else min(args.e2e_chunk, wl.s_q)},
             "gpu_launches": K * api.dsa_kernels_per_call(),
             "clocks": clocks}
+    if warm_ms is not None:
+        line["warm_l2"] = {"ms_per_step": warm_ms, "value": world * total / (warm_ms * 1e-3) / 1e12, "unit": UNIT,
+                           "note": "the same steps without the L2 flush between them (not the headline)"}
     if proj:
         line["config"]["d_model"] = wl.meta["d_model"]
         line["config"]["step"] = "forward, then y = out . W_o + x (cuBLASLt GEMM, not counted in gpu_launches)"
