@@ -153,10 +153,10 @@ def _measured_traffic(workload: str):
         return None
     with open(path) as f:
         rec = json.load(f)
-    if rec.get("kernel_sources_sha256") != _kernel_sources_sha256():
-        return None
     w = rec.get("workloads", {}).get(workload)
-    return None if w is None else float(w["dram_read_bytes"] + w["dram_write_bytes"])
+    if w is None or w.get("kernel_sources_sha256", rec.get("kernel_sources_sha256")) != _kernel_sources_sha256():
+        return None  # a capture of other kernel sources does not describe this build
+    return float(w["dram_read_bytes"] + w["dram_write_bytes"])
 
 
 def cpu_oracle_sample(wl, seconds: float, start_token: int = 0):

@@ -123,7 +123,7 @@ DSA_API dsa_status dsa_sparse_attn_fwd_fp8kv(const void* q, const void* kv_fp8, 
  * that is handed only its input and output buffers).  The pages have no
  * counterpart; this is a convenience of this library.  Arguments as for
  * dsa_sparse_attn_fwd, without the workspace: the call uses one scratch
- * array compiled into the library instead (about 40 MiB per device, held by
+ * array compiled into the library instead (about 43 MiB per device, held by
  * every GPU that loads the library until the process exits).
  * Limits: s_q <= 8192, h_q <= 128, and at most 80 resident SM pairs on the
  * device; larger calls return DSA_ERR_WORKSPACE and launch nothing.

@@ -56,6 +56,11 @@ __global__ void __launch_bounds__(kPrepWarps * 32) dsa_prep_kernel(const FwdPara
     for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
     if (lane == 0) nvalid[t] = c;
   }
+  if (p.dyn) {  // the per-pair token records start empty
+    const size_t n = (size_t)p.npairs * (size_t)(s_q + 1);
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x)
+      p.seq[i] = 0;
+  }
   __threadfence();
   __syncthreads();
   if (threadIdx.x == 0) is_last = (atomicAdd(&ctrl[kCtrlTicket], 1) == (int)gridDim.x - 1);
@@ -125,7 +130,8 @@ __global__ void __launch_bounds__(kCombineWarps * 32) dsa_combine_kernel(const i
                                                                          const int* __restrict__ ctrl, int s_q, int h_q,
                                                                          int npairs, const float* __restrict__ part_lse,
                                                                          const float* __restrict__ part_o, uint16_t* out,
-                                                                         float* lse) {
+                                                                         float* lse, int dyn) {
+  if (dyn) return;  // whole tokens only: nothing was split
   __shared__ int tok_s;
   __shared__ long long c0_s, c1_s;
   const int p = blockIdx.x;
@@ -263,6 +269,8 @@ static dsa_status forward(int kv_format, const void* q, const void* kv, const in
   p.ctrl = (int*)(ws + L.ctrl);
   p.nvalid = (int*)(ws + L.nvalid);
   p.cum = (int*)(ws + L.cum);
+  p.seq = (int*)(ws + L.seq);
+  p.dyn = s_q >= kDynTokensPerPair * npairs ? 1 : 0;
   p.part_lse = (float*)(ws + L.part_lse);
   p.part_o = (float*)(ws + L.part_o);
   p.npairs = npairs;
@@ -282,7 +290,7 @@ static dsa_status forward(int kv_format, const void* q, const void* kv, const in
   if (e != cudaSuccess) return DSA_ERR_CUDA;
   const dim3 cgrid((unsigned)npairs, (unsigned)((h_q + kCombineWarps - 1) / kCombineWarps));
   dsa_combine_kernel<<<cgrid, kCombineWarps * 32, 0, stream>>>(p.cum, p.ctrl, s_q, h_q, npairs, p.part_lse, p.part_o,
-                                                               (uint16_t*)out, lse);
+                                                               (uint16_t*)out, lse, p.dyn);
   return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
 

@@ -27,9 +27,11 @@
 //     reads: 16 KB chunks of 128 rows x 64 columns (K-major) on the QK side,
 //     16 KB row groups of 16 rows x 512 columns (MN-major) on the PV side.
 //     FP8 rows are first staged raw in a small ring, then dequantised.
-//   * Work: the index blocks of all tokens form one sequence; pair p takes the
-//     contiguous range [p*T/P, (p+1)*T/P).  A token cut by a range boundary is
-//     written as normalised partials and merged by the combine kernel.
+//   * Work: with at least 8 tokens per pair, pairs take whole tokens from a
+//     shared counter as they go, so that pairs on slower SMs take fewer.  With
+//     fewer tokens (decode), the index blocks of all tokens form one sequence and
+//     pair p takes the contiguous range [p*T/P, (p+1)*T/P); a token cut by a range
+//     boundary is written as normalised partials and merged by the combine kernel.
 //
 // Warp roles (512 threads, both CTAs): warp 0 compacts the valid indices of
 // each block into a small ring of index lists; warp 2 issues tcgen05.mma;
@@ -397,6 +399,117 @@ __device__ __forceinline__ uint32_t blocks_of_pair(const FwdParams& p, int pair)
   return (uint32_t)((long long)(pair + 1) * T / p.npairs - (long long)pair * T / p.npairs);
 }
 
+// Index blocks of token t (at least one, so that a token without valid slots still gets its output).
+__device__ __forceinline__ int blocks_of_token(const FwdParams& p, int t) {
+  const int nv = p.nvalid[t];
+  return nv > 0 ? (nv + kBT - 1) / kBT : 1;
+}
+
+// Dynamic token scheduling (p.dyn): the pair's i-th token is taken from the shared counter by the first
+// role that needs it, the QK side's index compactor, and recorded in seq[pair][i] (t + 1, or -1 when none
+// is left); every other role of both CTAs reads the record, waiting (bounded) until it is written.
+__device__ __forceinline__ int ld_acquire_gpu(const int* a) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(a) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_gpu(int* a, int v) {
+  asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(a), "r"(v) : "memory");
+}
+// Record i of this pair: t + 1, -1 (no more tokens) or 0 (the wait gave up).  One thread.
+__device__ __forceinline__ int token_record(const Ctx& c, const FwdParams& p, int i, bool take) {
+  int* e = p.seq + (size_t)c.pair * (size_t)(p.s_q + 1) + i;
+  if (take) {
+    const int t = atomicAdd(p.ctrl + kCtrlNextToken, 1);
+    const int v = t < p.s_q ? t + 1 : -1;
+    st_release_gpu(e, v);
+    return v;
+  }
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    const int v = ld_acquire_gpu(e);
+    if (v != 0) return v;
+    if ((it & 63u) == 0 && (*c.abort_flag || globaltimer_ns() - t0 > kWaitLimitNs)) return 0;
+  }
+}
+
+// The pieces of a pair: its static share, or whole tokens taken one by one.  next() runs on one thread;
+// next_warp() is called by all 32 lanes together: lane 0 takes or reads the record and the warp gets its
+// value by a shuffle, so every lane sees the same sequence even when a wait gives up.  `err` is set when
+// a wait gave up.
+struct WorkIter {
+  PieceIter st;
+  int i;
+  bool dyn, take;
+  __device__ void init(const Ctx& c, const FwdParams& p, bool taker) {
+    dyn = p.dyn != 0;
+    take = taker && c.rank == 0;
+    i = 0;
+    if (!dyn) st.init(p.cum, p.s_q, c.pair, p.npairs);
+  }
+  __device__ bool from_record(const FwdParams& p, int v, Piece& pc, bool& err) {
+    if (v == 0) {
+      err = true;
+      return false;
+    }
+    if (v < 0) return false;
+    pc.t = v - 1;
+    pc.lb0 = 0;
+    pc.lb1 = blocks_of_token(p, pc.t);
+    pc.full = true;
+    pc.slot = 0;
+    return true;
+  }
+  __device__ bool next(const Ctx& c, const FwdParams& p, Piece& pc, bool& err) {
+    if (!dyn) return st.next(pc);
+    return from_record(p, token_record(c, p, i++, take), pc, err);
+  }
+  __device__ bool next_warp(const Ctx& c, const FwdParams& p, Piece& pc, bool& err) {
+    if (!dyn) return st.next(pc);
+    int v = 0;
+    if (c.lane == 0) v = token_record(c, p, i, take);
+    v = __shfl_sync(0xffffffffu, v, 0);
+    ++i;
+    return from_record(p, v, pc, err);
+  }
+};
+
+// Whether block b of the pair exists, for the roles that walk blocks rather than tokens.  Static: b is
+// below the share's count.  Dynamic: the count grows as token records are read.  With `whole_warp`, all
+// 32 lanes call has() together and lane 0 reads each record for the warp (one shuffle per record).
+struct BlockCount {
+  uint32_t known;
+  int i;
+  bool more, warp;
+  __device__ void init(const Ctx& c, const FwdParams& p, bool whole_warp) {
+    more = p.dyn != 0;
+    warp = whole_warp;
+    i = 0;
+    known = more ? 0u : blocks_of_pair(p, c.pair);
+  }
+  __device__ bool has(const Ctx& c, const FwdParams& p, uint32_t b, bool& err) {
+    while (b >= known && more) {
+      int v;
+      if (warp) {
+        v = 0;
+        if (c.lane == 0) v = token_record(c, p, i, false);
+        v = __shfl_sync(0xffffffffu, v, 0);
+        ++i;
+      } else {
+        v = token_record(c, p, i++, false);
+      }
+      if (v <= 0) {
+        more = false;
+        if (v == 0) err = true;
+        break;
+      }
+      known += (uint32_t)blocks_of_token(p, v - 1);
+    }
+    return b < known;
+  }
+};
+
+
 // ============================================================================ both sides: index lists
 // Warp 0: walks this pair's pieces, compacts the valid slots of each block in
 // order and publishes them (row ids + count) in a ring of kIdxSlots lists.
@@ -405,12 +518,12 @@ __device__ void index_compactor(const Ctx& c, const FwdParams& p) {
   using Y = Lay<kFmt>;
   IndexRing ir;
   int* lists = (int*)(c.smem + Y::OffIdx);
-  PieceIter it;
-  it.init(p.cum, p.s_q, c.pair, p.npairs);
+  WorkIter it;
+  it.init(c, p, true);
   Piece pc;
   uint32_t b = 0;
-  bool ok = true;
-  while (ok && it.next(pc)) {
+  bool ok = true, err = false;
+  while (ok && it.next_warp(c, p, pc, err)) {
     ir.reset((int*)(c.smem + Y::OffRing), p, pc.t);
     for (int jb = 0; jb < pc.lb1; ++jb) {
       const int cnt = ir.fill(c.lane);
@@ -431,7 +544,7 @@ __device__ void index_compactor(const Ctx& c, const FwdParams& p) {
       ir.pop(cnt);
     }
   }
-  if (!ok) set_abort(c);
+  if (!ok || err) set_abort(c);
 }
 
 // ============================================================================ QK side
@@ -446,14 +559,15 @@ static __device__ void qk_gather_q(const Ctx& c, const FwdParams& p) {
   const int gt = gw * 32 + lane;
   constexpr int kGT = kGatherWarpsA * 32;
   const int* lists = (const int*)(smem + Y::OffIdx);
-  const uint32_t nblk = blocks_of_pair(p, c.pair);
-  bool ok = true;
+  BlockCount bc;
+  bc.init(c, p, true);
+  bool ok = true, err = false;
   {
     // Per block R::kUnits raw units of 128 rows x 64 bytes: latent code units (one 64-channel chunk of
     // e4m3, or two of e2m1) and the two rope halves (bf16); the block's scales ride with unit 0.  Units
     // are staged in a 4-slot ring two units ahead, then dequantised (latent) or copied (rope) into the
     // swizzled K chunk ring.
-    const uint32_t nunits = nblk * (uint32_t)R::kUnits;
+    auto exists = [&](uint32_t u) -> bool { return bc.has(c, p, u / (uint32_t)R::kUnits, err); };
     auto issue = [&](uint32_t u) -> bool {
       const uint32_t b = u / (uint32_t)R::kUnits;
       const int k = (int)(u % (uint32_t)R::kUnits), rs = (int)(u % kRawSlots);
@@ -525,12 +639,12 @@ static __device__ void qk_gather_q(const Ctx& c, const FwdParams& p) {
       if (k == R::kUnits - 1 && lane == 0) mbar_arrive(c.bar(IDX_EMPTY + (int)(b % kIdxSlots)));
       return true;
     };
-    for (uint32_t u = 0; u < 2u && u < nunits && ok; ++u) ok = issue(u);
-    for (uint32_t u = 0; u < nunits && ok; ++u) {
-      if (u + 2u < nunits) ok = issue(u + 2u);
+    for (uint32_t u = 0; u < 2u && ok && exists(u); ++u) ok = issue(u);
+    for (uint32_t u = 0; ok && exists(u); ++u) {
+      if (exists(u + 2u)) ok = issue(u + 2u);
       if (ok) ok = consume(u);
     }
-    if (!ok) set_abort(c);
+    if (!ok || err) set_abort(c);
   }
 }
 
@@ -542,10 +656,11 @@ static __device__ void qk_issue_bf16(const Ctx& c, const FwdParams& p) {
   using Y = Lay<kFmtBf16>;
   const int lane = c.lane, i = c.warp - 12;
   const int* lists = (const int*)(c.smem + Y::OffIdx);
-  const uint32_t nblk = blocks_of_pair(p, c.pair);
+  BlockCount bc;
+  bc.init(c, p, true);
   uint32_t issued = 0;
-  bool ok = true;
-  for (uint32_t b = 0; b < nblk && ok; ++b) {
+  bool ok = true, err = false;
+  for (uint32_t b = 0; ok && bc.has(c, p, b, err); ++b) {
     const int slot = (int)(b % kIdxSlots);
     if (!wait(c, IDX_FULL + slot, (b / kIdxSlots) & 1u)) { ok = false; break; }
     const int* l = lists + slot * kIdxSlotInts;
@@ -575,7 +690,7 @@ static __device__ void qk_issue_bf16(const Ctx& c, const FwdParams& p) {
     __syncwarp();
     if (lane == 0) mbar_arrive(c.bar(IDX_EMPTY + slot));
   }
-  if (!ok) set_abort(c);
+  if (!ok || err) set_abort(c);
   // the copies of the last block issued land before the CTA may exit
   if (issued > 0)
     for (int g = i; g < 2 * kGroupsPerHalf; g += kIssuersA)
@@ -587,9 +702,10 @@ static __device__ void qk_issue_bf16(const Ctx& c, const FwdParams& p) {
 static __device__ void qk_transpose_bf16(const Ctx& c, const FwdParams& p) {
   using Y = Lay<kFmtBf16>;
   const int lane = c.lane, t = (c.warp == 1) ? 0 : 1;
-  const uint32_t nblk = blocks_of_pair(p, c.pair);
-  bool ok = true;
-  for (uint32_t b = 0; b < nblk && ok; ++b) {
+  BlockCount bc;
+  bc.init(c, p, true);
+  bool ok = true, err = false;
+  for (uint32_t b = 0; ok && bc.has(c, p, b, err); ++b) {
     for (int g = t; g < 2 * kGroupsPerHalf; g += kTransA) {
       const int h = g / kGroupsPerHalf, gg = g % kGroupsPerHalf;
       if (!wait(c, A_LAND + g, b & 1u)) { ok = false; break; }
@@ -599,7 +715,7 @@ static __device__ void qk_transpose_bf16(const Ctx& c, const FwdParams& p) {
       if (lane == 0) mbar_arrive(c.bar(A_KH_FULL + h));
     }
   }
-  if (!ok) set_abort(c);
+  if (!ok || err) set_abort(c);
 }
 
 template <int kFmt>
@@ -607,13 +723,13 @@ __device__ void qk_mma(const Ctx& c, const FwdParams& p) {
   using Y = Lay<kFmt>;
   constexpr bool kQuant = kFmt != kFmtBf16;
   if (c.lane == 0) {
-    PieceIter it;
-    it.init(p.cum, p.s_q, c.pair, p.npairs);
+    WorkIter it;
+    it.init(c, p, false);
     Piece pc;
     uint32_t cseq = 0, blk = 0, item = 0;
-    bool ok = true;
+    bool ok = true, err = false;
     const uint32_t qrope = c.sbase + Y::A_OffQRope;
-    while (ok && it.next(pc)) {
+    while (ok && it.next(c, p, pc, err)) {
       const int nb = pc.lb1 - pc.lb0;
       if (!wait(c, A_Q_FULL, item & 1u)) { ok = false; break; }
       for (int j = 0; j < nb && ok; ++j, ++blk) {
@@ -668,7 +784,7 @@ __device__ void qk_mma(const Ctx& c, const FwdParams& p) {
       mma_commit(c.bar(A_Q_FREE));
       ++item;
     }
-    if (!ok) set_abort(c);
+    if (!ok || err) set_abort(c);
     mma_commit(c.bar(A_DRAIN));
     mbar_wait(c.bar(A_DRAIN), 0, kWaitLimitNs, nullptr);
   }
@@ -689,12 +805,12 @@ __device__ void qk_softmax(const Ctx& c, const FwdParams& p) {
   const uint32_t peer_msg = mapa_shared(c.sbase + Y::B_OffMsg, c.peer);
   const uint32_t peer_pin_full = mapa_shared(c.bars + 8u * (uint32_t)B_PIN_FULL, c.peer);
   const float sg = p.scale_log2 < 0.f ? -1.f : 1.f;  // direction the scale preserves
-  PieceIter it;
-  it.init(p.cum, p.s_q, c.pair, p.npairs);
+  WorkIter it;
+  it.init(c, p, false);
   Piece pc;
   uint32_t blk = 0, item = 0, nsync = 0;
-  bool ok = true;
-  while (ok && it.next(pc)) {
+  bool ok = true, err = false;
+  while (ok && it.next_warp(c, p, pc, err)) {
     const int nb = pc.lb1 - pc.lb0;
     const int nval = p.nvalid[pc.t];
     // ---- Q for this token: latent columns [256*half, +256) into TMEM, rope (half 0) into smem
@@ -824,7 +940,7 @@ __device__ void qk_softmax(const Ctx& c, const FwdParams& p) {
     }
     ++item;
   }
-  if (!ok && lane == 0) set_abort(c);
+  if ((!ok || err) && lane == 0) set_abort(c);
 }
 
 // ============================================================================ PV side
@@ -839,12 +955,13 @@ static __device__ void pv_gather_q(const Ctx& c, const FwdParams& p) {
   const int gt = gw * 32 + lane;
   constexpr int kGT = kGatherWarpsB * 32;
   const int* lists = (const int*)(smem + Y::OffIdx);
-  const uint32_t nblk = blocks_of_pair(p, c.pair);
-  bool ok = true;
+  BlockCount bc;
+  bc.init(c, p, true);
+  bool ok = true, err = false;
   {
     // Per 16-row group one raw unit: the codes and scales at the start of each row (528 bytes for FP8,
     // 320 for FP4), staged two units ahead, then dequantised into the MN-major V row-group ring.
-    const uint32_t nunits = nblk * (uint32_t)kGroupsPerBlock;
+    auto exists = [&](uint32_t u) -> bool { return bc.has(c, p, u / (uint32_t)kGroupsPerBlock, err); };
     auto issue = [&](uint32_t u) -> bool {
       const uint32_t b = u / (uint32_t)kGroupsPerBlock;
       const int g = (int)(u % (uint32_t)kGroupsPerBlock), rs = (int)(u % kRawSlots);
@@ -895,12 +1012,12 @@ static __device__ void pv_gather_q(const Ctx& c, const FwdParams& p) {
       if (g == kGroupsPerBlock - 1 && lane == 0) mbar_arrive(c.bar(IDX_EMPTY + (int)(b % kIdxSlots)));
       return true;
     };
-    for (uint32_t u = 0; u < 2u && u < nunits && ok; ++u) ok = issue(u);
-    for (uint32_t u = 0; u < nunits && ok; ++u) {
-      if (u + 2u < nunits) ok = issue(u + 2u);
+    for (uint32_t u = 0; u < 2u && ok && exists(u); ++u) ok = issue(u);
+    for (uint32_t u = 0; ok && exists(u); ++u) {
+      if (exists(u + 2u)) ok = issue(u + 2u);
       if (ok) ok = consume(u);
     }
-    if (!ok) set_abort(c);
+    if (!ok || err) set_abort(c);
   }
 }
 
@@ -910,10 +1027,11 @@ static __device__ void pv_issue_bf16(const Ctx& c, const FwdParams& p) {
   using Y = Lay<kFmtBf16>;
   const int lane = c.lane, i = c.warp - 8;
   const int* lists = (const int*)(c.smem + Y::OffIdx);
-  const uint32_t nblk = blocks_of_pair(p, c.pair);
+  BlockCount bc;
+  bc.init(c, p, true);
   uint32_t done = 0;  // groups of all blocks before the current one
-  bool ok = true;
-  for (uint32_t b = 0; b < nblk && ok; ++b) {
+  bool ok = true, err = false;
+  for (uint32_t b = 0; ok && bc.has(c, p, b, err); ++b) {
     const int slot = (int)(b % kIdxSlots);
     if (!wait(c, IDX_FULL + slot, (b / kIdxSlots) & 1u)) { ok = false; break; }
     const int* l = lists + slot * kIdxSlotInts;
@@ -937,7 +1055,7 @@ static __device__ void pv_issue_bf16(const Ctx& c, const FwdParams& p) {
     __syncwarp();
     if (lane == 0) mbar_arrive(c.bar(IDX_EMPTY + slot));
   }
-  if (!ok) set_abort(c);
+  if (!ok || err) set_abort(c);
   // the copies of the last ring round land before the CTA may exit
   for (uint32_t gs = done > (uint32_t)Y::kVSlots ? done - Y::kVSlots : 0u; gs < done; ++gs)
     if ((int)(gs % (uint32_t)kGroupsPerBlock) % kIssuersB == i)
@@ -948,9 +1066,10 @@ static __device__ void pv_issue_bf16(const Ctx& c, const FwdParams& p) {
 static __device__ void pv_transpose_bf16(const Ctx& c, const FwdParams& p) {
   using Y = Lay<kFmtBf16>;
   const int lane = c.lane, t = (c.warp == 1) ? 0 : c.warp - 13;
-  const uint32_t total = blocks_of_pair(p, c.pair) * (uint32_t)kGroupsPerBlock;
-  bool ok = true;
-  for (uint32_t gs = (uint32_t)t; gs < total; gs += kTransB) {
+  BlockCount bc;
+  bc.init(c, p, true);
+  bool ok = true, err = false;
+  for (uint32_t gs = (uint32_t)t; bc.has(c, p, gs / (uint32_t)kGroupsPerBlock, err); gs += kTransB) {
     const int s = (int)(gs % Y::kVSlots);
     if (!wait(c, B_V_LAND + s, (gs / Y::kVSlots) & 1u)) { ok = false; break; }
     const uint32_t grp = c.sbase + Y::B_OffV + (uint32_t)(s * kVGroupBytes);
@@ -960,7 +1079,7 @@ static __device__ void pv_transpose_bf16(const Ctx& c, const FwdParams& p) {
     __syncwarp();
     if (lane == 0) mbar_arrive(c.bar(B_V_FULL + s));
   }
-  if (!ok) set_abort(c);
+  if (!ok || err) set_abort(c);
 }
 
 template <int kFmt>
@@ -968,12 +1087,12 @@ __device__ void pv_mma(const Ctx& c, const FwdParams& p) {
   using Y = Lay<kFmt>;
   constexpr bool kQuant = kFmt != kFmtBf16;
   if (c.lane == 0) {
-    PieceIter it;
-    it.init(p.cum, p.s_q, c.pair, p.npairs);
+    WorkIter it;
+    it.init(c, p, false);
     Piece pc;
     uint32_t gseq = 0, blk = 0, item = 0;
-    bool ok = true;
-    while (ok && it.next(pc)) {
+    bool ok = true, err = false;
+    while (ok && it.next(c, p, pc, err)) {
       const int nb = pc.lb1 - pc.lb0;
       for (int j = 0; j < nb && ok; ++j, ++blk) {
         const int pb = (int)(blk & 1u);
@@ -1006,7 +1125,7 @@ __device__ void pv_mma(const Ctx& c, const FwdParams& p) {
       }
       ++item;
     }
-    if (!ok) set_abort(c);
+    if (!ok || err) set_abort(c);
     mma_commit(c.bar(B_DRAIN));
     mbar_wait(c.bar(B_DRAIN), 0, kWaitLimitNs, nullptr);
   }
@@ -1018,18 +1137,19 @@ __device__ __forceinline__ void pv_slot_return(const Ctx& c, const FwdParams& p)
   if (c.lane == 0) {
     const uint32_t peer_pout_empty = mapa_shared(c.bars + 8u * (uint32_t)A_POUT_EMPTY, c.peer);
     const uint32_t peer_msg_free = mapa_shared(c.bars + 8u * (uint32_t)A_MSG_FREE, c.peer);
-    const uint32_t nblk = blocks_of_pair(p, c.pair);
-    bool ok = true;
-    for (uint32_t b = 0; b < nblk && b < 2; ++b) mbar_arrive_expect_tx(c.bar(B_PIN_FULL + (int)b), kMsgBytes);
-    for (uint32_t b = 0; b < nblk; ++b) {
+    BlockCount bc;
+    bc.init(c, p, false);
+    bool ok = true, err = false;
+    for (uint32_t b = 0; b < 2 && bc.has(c, p, b, err); ++b) mbar_arrive_expect_tx(c.bar(B_PIN_FULL + (int)b), kMsgBytes);
+    for (uint32_t b = 0; bc.has(c, p, b, err); ++b) {
       const int pb = (int)(b & 1u);
       if (!wait(c, B_PIN_FULL + pb, (b >> 1) & 1u)) { ok = false; break; }
       mbar_arrive_remote(peer_msg_free);  // the QK side may refill its outgoing buffer
       if (!wait(c, B_PV_DONE + pb, (b >> 1) & 1u)) { ok = false; break; }
-      if (b + 2 < nblk) mbar_arrive_expect_tx(c.bar(B_PIN_FULL + pb), kMsgBytes);
+      if (bc.has(c, p, b + 2, err)) mbar_arrive_expect_tx(c.bar(B_PIN_FULL + pb), kMsgBytes);
       mbar_arrive_remote(peer_pout_empty + 8u * (uint32_t)pb);
     }
-    if (!ok) set_abort(c);
+    if (!ok || err) set_abort(c);
   }
   __syncwarp();
 }
@@ -1042,12 +1162,12 @@ __device__ void pv_epilogue(const Ctx& c, const FwdParams& p) {
   const int quarter = c.warp & 3;
   const int r = quarter * 32 + lane;
   const uint32_t trow = c.tmem + ((uint32_t)(quarter * 32) << 16);
-  PieceIter it;
-  it.init(p.cum, p.s_q, c.pair, p.npairs);
+  WorkIter it;
+  it.init(c, p, false);
   Piece pc;
   uint32_t blk = 0, item = 0;
-  bool ok = true;
-  while (ok && it.next(pc)) {
+  bool ok = true, err = false;
+  while (ok && it.next_warp(c, p, pc, err)) {
     const int nb = pc.lb1 - pc.lb0;
     float inv = 0.f, lse_val = -INFINITY;
     for (int j = 0; j < nb; ++j, ++blk) {
@@ -1119,7 +1239,7 @@ __device__ void pv_epilogue(const Ctx& c, const FwdParams& p) {
     if (lane == 0) mbar_arrive(c.bar(B_O_FREE));
     ++item;
   }
-  if (!ok && lane == 0) set_abort(c);
+  if ((!ok || err) && lane == 0) set_abort(c);
 }
 
 }  // namespace fwd

@@ -14,11 +14,16 @@ constexpr int kMaxHeads = 128;   // the MMA M dimension; smaller h_q is padded
 constexpr int kFp8RowBytes = 656;
 
 // Workspace layout.  ctrl[] words:
-enum CtrlWord { kCtrlStatus = 0, kCtrlTicket = 1, kCtrlTotalBlocks = 2, kCtrlWords = 64 };
+enum CtrlWord { kCtrlStatus = 0, kCtrlTicket = 1, kCtrlTotalBlocks = 2, kCtrlNextToken = 3, kCtrlWords = 64 };
 
 struct WorkspaceLayout {
-  size_t ctrl, nvalid, cum, part_lse, part_o, total;
+  size_t ctrl, nvalid, cum, seq, part_lse, part_o, total;
 };
+
+// Token scheduling: with at least this many tokens per SM pair, pairs take whole tokens from a shared
+// counter as they go (so a pair on a slower SM takes fewer); below it, each pair gets an equal static
+// share of the index blocks and tokens cut by a share boundary are merged afterwards.
+constexpr int kDynTokensPerPair = 8;
 
 constexpr size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -28,6 +33,7 @@ constexpr WorkspaceLayout workspace_layout(int s_q, int h_q, int npairs) {
   L.ctrl = off;     off += 256;
   L.nvalid = off;   off += align_up(sizeof(int) * (size_t)(s_q > 0 ? s_q : 1), 256);
   L.cum = off;      off += align_up(sizeof(int) * (size_t)(s_q + 1), 256);
+  L.seq = off;      off += align_up(sizeof(int) * (size_t)npairs * (size_t)(s_q + 1), 256);
   L.part_lse = off; off += align_up(sizeof(float) * 2 * (size_t)npairs * h_q, 256);
   L.part_o = off;   off += align_up(sizeof(float) * 2 * (size_t)npairs * h_q * kDV, 256);
   L.total = off;
@@ -56,6 +62,8 @@ struct FwdParams {
   int* ctrl;
   int* nvalid;               // [s_q] valid slots per token
   int* cum;                  // [s_q + 1] prefix sum of index blocks per token
+  int* seq;                  // [npairs][s_q + 1] tokens each pair took, in order, as t + 1; -1 = none left
+  int dyn;                   // 1: pairs take whole tokens from ctrl[kCtrlNextToken]; 0: static shares
   float* part_lse;           // [2 * npairs, h_q]
   float* part_o;             // [2 * npairs, h_q, 512]
   int npairs;

@@ -14,7 +14,7 @@ namespace dsa {
 
 // Limits of the built-in scratch: up to 8192 query tokens, 128 heads and 80 SM
 // pairs (a GB300 has 76).  The split-token partial outputs dominate its size
-// (about 40 MiB); every GPU that loads the library keeps it until the process exits.
+// (about 43 MiB); every GPU that loads the library keeps it until the process exits.
 constexpr int kNoAllocMaxTokens = 8192;
 constexpr int kNoAllocMaxPairs = 80;
 constexpr size_t kNoAllocScratchBytes = workspace_layout(kNoAllocMaxTokens, kMaxHeads, kNoAllocMaxPairs).total;

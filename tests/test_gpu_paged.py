@@ -76,3 +76,13 @@ def test_decode_paged_full_size_sampled():
     wl = W.decode_paged()
     out, lse = P.run_gpu_paged(wl)
     _check(wl, tokens=[0, 1, 30, 63], out=out, lse=lse)
+
+
+def test_paged_dynamic_token_scheduling():
+    # 640 tokens: pairs take whole tokens from the shared counter
+    wl = W.small_paged(81, 640, 16, 8, 12, 32, 200, unmapped_frac=0.1, invalid_frac=0.05)
+    out, lse = P.run_gpu_paged(wl)
+    tokens = list(range(0, 640, 29))
+    ref_out, ref_lse = P.oracle_paged(wl, tokens)
+    ok, rep = P.compare(out[tokens], lse[tokens], ref_out, ref_lse, wl.kv_format)
+    assert ok, rep

@@ -193,3 +193,32 @@ def test_decode_fp4_full_size_sampled():
     wl = W.decode_fp4()
     out, lse = P.run_gpu(wl)
     _check(wl, tokens=[0, 1, 50, 99, 127], out=out, lse=lse)
+
+
+# ---------------------------------------------------------------- whole tokens taken from a shared counter
+# With at least 8 tokens per SM pair the pairs take whole tokens one by one instead of static shares
+# (76 pairs on a GB300: from 608 tokens on).
+
+@pytest.mark.parametrize("kv_format", ["bf16", "fp8"])
+def test_dynamic_token_scheduling(kv_format):
+    wl = W.small_random(71, 700, 16, 3000, 300, kv_format=kv_format, invalid_frac=0.05,
+                        q_sigma=2.0 if kv_format != "bf16" else 1.0)
+    wl.indices[5] = -1      # a token with no valid slot
+    wl.indices[6, 1:] = -1  # a token with one valid slot
+    _check(wl, tokens=list(range(0, 700, 23)) + [5, 6, 699])
+
+
+def test_dynamic_scheduling_is_repeatable_and_complete():
+    from sparse_mla_attention_dsa_gb300 import api
+    wl = W.small_random(72, 1000, 16, 2000, 130)
+    q, kv, idx = wl.q.cuda(), wl.kv.cuda(), wl.indices.cuda()
+    out = torch.full((wl.s_q, wl.h_q, 512), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lse = torch.full((wl.s_q, wl.h_q), float("nan"), device="cuda")
+    api.dsa_sparse_attn_fwd(q, kv, idx, wl.sm_scale, out=out, lse=lse, check_status=True)
+    o1, l1 = out.clone(), lse.clone()
+    assert not torch.isnan(o1.float()).any() and not torch.isnan(l1).any()  # every token written
+    api.dsa_sparse_attn_fwd(q, kv, idx, wl.sm_scale, out=out, lse=lse, check_status=True)
+    torch.cuda.synchronize()
+    # a token's result does not depend on which pair took it
+    assert torch.equal(o1.view(torch.int16), out.view(torch.int16)) and torch.equal(l1, lse)
+    _check(wl, tokens=range(0, 1000, 37), out=o1, lse=l1)
