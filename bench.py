@@ -155,7 +155,7 @@ def _measured_traffic(workload: str):
         rec = json.load(f)
     w = rec.get("workloads", {}).get(workload)
     if w is None or w.get("kernel_sources_sha256", rec.get("kernel_sources_sha256")) != _kernel_sources_sha256():
-        return None  # a capture of other kernel sources does not describe this build
+        return None  # a capture of other kernel sources does not describe the compiled kernel
     return float(w["dram_read_bytes"] + w["dram_write_bytes"])
 
 

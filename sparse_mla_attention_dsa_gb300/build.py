@@ -1,9 +1,9 @@
 """Builds the CUDA library (sm_103a) in-tree with nvcc.
 
 Each translation unit in csrc/ is compiled in parallel, then linked into
-``_build/libdsa_gb300.so``.  The CUDA runtime is linked statically and the
-driver's tensor-map encoder is looked up at run time, so the library loads on
-a machine without a GPU driver (every call then reports an error).
+``_build/libdsa_gb300.so``.  The CUDA runtime is linked statically and cuBLASLt
+(the output projection's GEMM) dynamically; the library loads on a machine
+without a GPU driver (every call that needs the device then reports an error).
 """
 from __future__ import annotations
 
