@@ -21,11 +21,13 @@ cudaError_t launch_fwd_fp4(const FwdParams& p, cudaStream_t stream);
 
 // ----------------------------------------------------------------------------
 // Scheduling: n_valid per token, then (by the last CTA to finish) the prefix
-// sum of index blocks per token, max(1, ceil(n_valid / 64)).  A token with no
+// sum of index blocks per token, max(1, ceil(n_valid / 128)).  A token with no
 // valid slot still owns one (fully masked) block, which writes out = 0 and
 // lse = -inf.  Per-CTA load balance follows the weight idea of
 // "Flash Attention Infer算子性能优化", section "优化多核负载均衡": work is
-// weighted by valid blocks, and the pairs take equal contiguous shares.
+// weighted by valid blocks.  With few tokens per SM pair the pairs take equal
+// contiguous shares of the block sequence; with many, they take whole tokens
+// from a shared counter, and this kernel clears the per-pair token records.
 // ----------------------------------------------------------------------------
 constexpr int kPrepWarps = 8;
 
