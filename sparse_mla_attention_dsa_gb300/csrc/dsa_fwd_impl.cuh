@@ -1,11 +1,12 @@
-// The sparse MLA forward kernel for sm_103a, templated on the KV format
-// (bf16 rows of 576 values, or FP8 rows of 512 e4m3 + 4 fp32 scales + 64 bf16).
+// The sparse MLA forward kernel for sm_103a, templated on the KV format: bf16
+// rows of 576 values, FP8 rows of 512 e4m3 + 4 fp32 scales + 64 bf16, or FP4
+// rows of 512 e2m1 + 16 fp32 scales + 64 bf16.
 //
 // Method: "Ascend Sparse Attention Forward 算法与优化技术简析", sections
 // "数学建模" (what is computed) and "计算流程" (blockwise online softmax with
 // skip-scale).  The page's delayed P@V order (section "流水线") survives as
 // a pipeline across two SMs; its index prefetch / multi-stage gather idea
-// survives as chunk rings fed by cp.async; its FP8 decoding (section
+// survives as rings of gathered rows; its FP8 decoding (section
 // "能不能用 1C1V": KV dequantised to bf16 before the matrix unit) is done by
 // the gather warps on their way into the swizzled operand layouts.
 //
@@ -22,11 +23,14 @@
 //       rescale factors, multiplies P by V and writes the normalised output.
 //     Tensor work per block is 576 vs 512 column-units, so the pair is
 //     balanced; only bf16 P crosses between the SMs (one way).
-//   * Gathers use cp.async (16 bytes per thread) with the address swizzled on
-//     the way in, straight into the 128-byte-swizzled layouts tcgen05.mma
-//     reads: 16 KB chunks of 128 rows x 64 columns (K-major) on the QK side,
-//     16 KB row groups of 16 rows x 512 columns (MN-major) on the PV side.
-//     FP8 rows are first staged raw in a small ring, then dequantised.
+//   * Gathers, bf16: one bulk copy per row lands the 1 KB latent part of 8 rows
+//     as an 8 KB unit, which one warp transposes in place into eight
+//     128-byte-swizzled atoms: the K-major operand of the QK side and the
+//     MN-major operand of the PV side are the same unit layout.  The rope part
+//     comes by cp.async straight into its swizzled atom.
+//     Quantised rows: cp.async (16 bytes per thread) into a small raw ring,
+//     dequantised by the same warps into 16 KB chunks of 128 rows x 64 columns
+//     (K-major, QK side) and 16-row groups of 512 columns (MN-major, PV side).
 //   * Work: with at least 8 tokens per pair, pairs take whole tokens from a
 //     shared counter as they go, so that pairs on slower SMs take fewer.  With
 //     fewer tokens (decode), the index blocks of all tokens form one sequence and
