@@ -21,6 +21,7 @@ namespace {
 
 constexpr size_t kLtWorkspace = 32u << 20;  // cuBLASLt workspace handed to every call
 constexpr int kMaxDevices = 64;
+constexpr size_t kMaxCachedAlgos = 256;  // distinct (device, shape) entries kept
 
 std::mutex g_mu;
 cublasLtHandle_t g_handle[kMaxDevices] = {};
@@ -106,6 +107,7 @@ dsa_status dsa_out_proj(const void* o, const void* w_o, const void* x, int s_q, 
       return DSA_ERR_UNSUPPORTED;
     algo = res.algo;
     std::lock_guard<std::mutex> lk(g_mu);
+    if (g_algos.size() >= kMaxCachedAlgos) g_algos.erase(g_algos.begin());  // bounded: oldest shape goes
     g_algos.push_back(AlgoEntry{dev, m, n, k, residual, kLtWorkspace, algo});
   }
   const float alpha = 1.f, beta = residual ? 1.f : 0.f;
