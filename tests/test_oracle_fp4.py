@@ -55,3 +55,25 @@ def test_fp4_product_is_rounded_to_bf16():
 def test_kv_dispatch_knows_fp4():
     row = _row({0: 4}, [1.0] * 16, 2.0)
     assert np.array_equal(O.kv_to_f64(row[None, :], "fp4"), F.fp4_rows_to_f64(row[None, :]))
+
+
+def test_fp4_definition_uses_dequantised_rows():
+    # the FP4 forward through the oracle equals a dense brute force over rows dequantised by a second route:
+    # the e2m1 value table above, scales repeated over their 32-channel groups, torch's bf16 rounding
+    from sparse_mla_attention_dsa_gb300 import workloads as W
+    from tests.test_oracle import _bits, _dense_torch
+    wl = W.small_random(43, 3, 16, 200, 70, kv_format="fp4", q_sigma=2.0)
+    rows = wl.kv.numpy()
+    q = O.q_to_f64(_bits(wl.q))
+    idx = wl.indices.numpy()
+    out, lse = O.sparse_mla_fwd(q, O.kv_to_f64(rows, "fp4"), idx, wl.sm_scale)
+    table = np.array(E2M1)
+    codes = np.stack([rows[:, :256] & 0xF, rows[:, :256] >> 4], axis=2).reshape(rows.shape[0], 512)
+    scales = rows[:, 256:320].copy().view(np.float32).astype(np.float64)
+    lat32 = (table[codes].astype(np.float32) * np.repeat(scales, 32, axis=1).astype(np.float32)).astype(np.float32)
+    lat = torch.from_numpy(lat32).to(torch.bfloat16).double().numpy()
+    rope = torch.from_numpy(rows[:, 320:].copy()).view(torch.bfloat16).double().numpy()
+    kv_t = np.concatenate([lat, rope], axis=1)
+    for t in range(3):
+        ro, rl = _dense_torch(q[t], kv_t, idx[t], wl.sm_scale)
+        assert np.allclose(out[t], ro, rtol=1e-11, atol=1e-12) and np.allclose(lse[t], rl, rtol=1e-12)
